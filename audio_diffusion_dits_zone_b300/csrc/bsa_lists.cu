@@ -1,0 +1,123 @@
+// Helpers of the block-sparse attention backward.
+//
+// transpose_lists: for every (head h, key block j) the query blocks i whose kept
+//   list contains j, ascending.  A bit matrix bits[h][j][i / 32] is set from the
+//   kept lists (atomicOr), then one warp per (h, j) emits the set bits in order
+//   (popcount + warp scan), so the result is deterministic.
+// row_dot: D[h][r] = sum_c dO[r, h, c] * O[r, h, c] (fp32), the softmax-gradient
+//   row term of dS = P * (dP - D).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace prism {
+namespace {
+
+size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+__global__ void set_bits_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ idx, int Hh, int nb,
+                                uint32_t* __restrict__ bits, uint32_t* status) {
+  const int words = (nb + 31) / 32;
+  const int row = blockIdx.x;  // h * nb + i
+  const int h = row / nb, i = row - h * nb;
+  const int cnt = counts[row];
+  const int32_t* lst = idx + (size_t)row * nb;
+  for (int t = threadIdx.x; t < cnt && t < nb; t += blockDim.x) {
+    const int j = lst[t];
+    if (j < 0 || j >= nb) {
+      flag_error(status, PRISM_DEV_BAD_INDEX);
+      continue;
+    }
+    atomicOr(&bits[((size_t)h * nb + j) * words + (i >> 5)], 1u << (i & 31));
+  }
+  if (threadIdx.x == 0 && (cnt < 0 || cnt > nb)) flag_error(status, PRISM_DEV_BAD_INDEX);
+}
+
+__global__ void emit_lists_kernel(const uint32_t* __restrict__ bits, int Hh, int nb, int32_t* __restrict__ tcounts,
+                                  int32_t* __restrict__ tidx) {
+  const int words = (nb + 31) / 32;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= Hh * nb) return;
+  const uint32_t* bw = bits + (size_t)warp * words;
+  int32_t* out = tidx + (size_t)warp * nb;
+  int base = 0;
+  for (int w0 = 0; w0 < words; w0 += 32) {
+    const uint32_t word = (w0 + lane < words) ? bw[w0 + lane] : 0u;
+    const int c = __popc(word);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int pos = base + incl - c;
+    uint32_t x = word;
+    while (x) {
+      const int b = __ffs(x) - 1;
+      out[pos++] = (w0 + lane) * 32 + b;
+      x &= x - 1;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) tcounts[warp] = base;
+}
+
+template <typename T>
+__global__ void row_dot_kernel(const T* __restrict__ o, const T* __restrict__ dO, int64_t ld, int N, int Hh, int d,
+                               float* __restrict__ D) {
+  // one warp per (token, head)
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= (int64_t)N * Hh) return;
+  const int64_t n = wid / Hh;
+  const int h = (int)(wid - n * Hh);
+  const T* a = o + n * ld + (int64_t)h * d;
+  const T* b = dO + n * ld + (int64_t)h * d;
+  float s = 0.f;
+  for (int c = lane; c < d; c += 32) s = fmaf(to_f32<T>(a[c]), to_f32<T>(b[c]), s);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) D[(size_t)h * N + n] = s;
+}
+
+}  // namespace
+
+size_t lists_ws_bytes(int Hh, int nb) {
+  const size_t words = (size_t)(nb + 31) / 32;
+  return a256((size_t)Hh * nb * words * 4) + a256((size_t)Hh * nb * 4) + a256((size_t)Hh * nb * nb * 4);
+}
+
+cudaError_t transpose_lists_launch(const int32_t* counts, const int32_t* idx, int Hh, int nb, void* ws,
+                                   int32_t** tcounts, int32_t** tidx, cudaStream_t st, uint32_t* status) {
+  const size_t words = (size_t)(nb + 31) / 32;
+  char* p = static_cast<char*>(ws);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(p);
+  p += a256((size_t)Hh * nb * words * 4);
+  *tcounts = reinterpret_cast<int32_t*>(p);
+  p += a256((size_t)Hh * nb * 4);
+  *tidx = reinterpret_cast<int32_t*>(p);
+  cudaError_t e = cudaMemsetAsync(bits, 0, (size_t)Hh * nb * words * 4, st);
+  if (e != cudaSuccess) return e;
+  set_bits_kernel<<<Hh * nb, 128, 0, st>>>(counts, idx, Hh, nb, bits, status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t threads = (int64_t)Hh * nb * 32;
+  emit_lists_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(bits, Hh, nb, *tcounts, *tidx);
+  return cudaGetLastError();
+}
+
+cudaError_t row_dot_launch(const void* o, const void* dO, int dtype, int64_t ld, int N, int Hh, int d, float* Drow,
+                           cudaStream_t st) {
+  const int64_t threads = (int64_t)N * Hh * 32;
+  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (dtype == PRISM_BF16)
+    row_dot_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
+                                                          static_cast<const __nv_bfloat16*>(dO), ld, N, Hh, d, Drow);
+  else
+    row_dot_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(o), static_cast<const float*>(dO), ld, N,
+                                                  Hh, d, Drow);
+  return cudaGetLastError();
+}
+
+}  // namespace prism

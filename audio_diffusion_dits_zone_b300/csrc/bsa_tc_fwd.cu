@@ -1,0 +1,495 @@
+// Step 4 of the path on the tensor cores: Prism Block Sparse Attention forward,
+// bf16 inputs, d = 128, 128-token blocks (sm_103a: TMA + tcgen05 + TMEM).
+//
+// "Prism: dynamic sparse attention for 2K joint video-audio generation training",
+// section "Region-adapted block construction", paragraph 2: attention runs only on
+// the blocks the hybrid selection kept for each query block.  For every query
+// token r of query block i and every token c of the kept blocks:
+//   O[r] = sum_c softmax_c(Q[r].K[c] / sqrt(d)) V[c],  lse[r] = log sum_c exp(Q[r].K[c] / sqrt(d)).
+//
+// One CTA per (head, query block), 7 warps with fixed roles:
+//   warp 0      TMA producer of K tiles (3-stage ring), walking the kept list;
+//   warp 6      TMA producer of the Q tile and of V tiles (3-stage ring);
+//   warp 1      TMEM owner and MMA issuer (one thread):
+//                 S_b = Q K_j^T   (A, B from shared memory, K-major, 128B swizzle)
+//                 O  += P_b V_j   (A = P from TMEM, B = V from shared memory, MN-major)
+//               S is double-buffered in TMEM so S(j+1) runs while the softmax of
+//               block j is computed; P (bf16) overwrites the S buffer it came from;
+//   warps 2-5   softmax: one thread per query row (its TMEM lane); online softmax in
+//               the log2 domain with ex2.approx; the O accumulator in TMEM is
+//               rescaled only when the running row max grows by more than 2^8
+//               (otherwise P is taken against the stale max, which bounds P by 256).
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384) of a 512-column allocation.
+// The kept lists give block coordinates directly (tokens are already in block
+// order), so gathering a key block is one TMA box coordinate.  Every wait is
+// bounded; on a timeout the CTA drains its copies and MMAs, frees TMEM and exits
+// with PRISM_DEV_TIMEOUT in the status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace prism {
+
+// ------------------------------------------------------------- tensor maps
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+}  // namespace
+
+bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_outer) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+constexpr int kBM = 128;   // query rows per tile
+constexpr int kBN = 128;   // key rows per tile
+constexpr int kD = 128;    // head dim
+constexpr int kStages = 3;
+constexpr uint32_t kHalf = 16384;          // one 128-row x 64-col bf16 box (128B swizzled)
+constexpr uint32_t kTile = 2 * kHalf;      // a 128 x 128 bf16 tile
+constexpr int kThreads = 224;
+constexpr float kSl2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+
+struct FwdSmem {
+  uint8_t q[kTile];
+  uint8_t k[kStages][kTile];
+  uint8_t v[kStages][kTile];
+  uint64_t q_full;
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_bar, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kFwdSmemBytes = sizeof(FwdSmem) + 1024;
+static_assert(kFwdSmemBytes <= 232448, "shared memory budget");
+
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// Load 32 TMEM columns of this thread's lane and wait for them.
+__device__ __forceinline__ void tmem_load_row32(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_ld32(taddr, r);
+  tmem_wait_ld();
+  reg_fence(r);
+}
+
+// Drain wait used on the way out: ignores the abort flag, bounded in time.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ int block_of(const int32_t* lst, int it, int nb, bool& ok) {
+  const int j = lst[it];
+  ok = (j >= 0 && j < nb);
+  return ok ? j : 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
+                      float* __restrict__ lse, int64_t ld, int N, const int32_t* __restrict__ counts,
+                      const int32_t* __restrict__ idx, int nb, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x;  // head * nb + query block
+  const int h = item / nb, i = item - h * nb;
+  int cnt = counts[item];
+  if (cnt < 0 || cnt > nb) {
+    if (threadIdx.x == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
+    cnt = cnt < 0 ? 0 : nb;
+  }
+  const int32_t* lst = idx + (size_t)item * nb;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[s]), 1);
+      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sm.s_full[b]), 1);
+      mbar_init(smem_u32(&sm.p_full[b]), 4);
+    }
+    mbar_init(smem_u32(&sm.o_bar), 1);
+    mbar_init(smem_u32(&sm.mma_done), 1);
+    sm.abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort = &sm.abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- K producer
+    if (lane == 0 && cnt > 0) {
+      tma_prefetch_desc(&tmk);
+      int armed[kStages] = {0, 0, 0};
+      for (int it = 0; it < cnt; ++it) {
+        const int st = it % kStages;
+        if (it >= kStages && !mbar_wait(smem_u32(&sm.k_empty[st]), ((it / kStages) - 1) & 1, abort, status)) break;
+        bool ok;
+        const int j = block_of(lst, it, nb, ok);
+        const uint32_t bar = smem_u32(&sm.k_full[st]);
+        mbar_arrive_expect_tx(bar, kTile);
+        tma_load_2d(smem_u32(sm.k[st]), &tmk, h * kD, j * kBN, bar);
+        tma_load_2d(smem_u32(sm.k[st]) + kHalf, &tmk, h * kD + 64, j * kBN, bar);
+        ++armed[st];
+      }
+      if (*abort)
+        for (int s = 0; s < kStages; ++s)
+          if (armed[s]) drain_wait(smem_u32(&sm.k_full[s]), (armed[s] - 1) & 1);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ Q / V producer
+    if (lane == 0 && cnt > 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmv);
+      const uint32_t qbar = smem_u32(&sm.q_full);
+      mbar_arrive_expect_tx(qbar, kTile);
+      tma_load_2d(smem_u32(sm.q), &tmq, h * kD, i * kBM, qbar);
+      tma_load_2d(smem_u32(sm.q) + kHalf, &tmq, h * kD + 64, i * kBM, qbar);
+      int armed[kStages] = {0, 0, 0};
+      for (int it = 0; it < cnt; ++it) {
+        const int st = it % kStages;
+        if (it >= kStages && !mbar_wait(smem_u32(&sm.v_empty[st]), ((it / kStages) - 1) & 1, abort, status)) break;
+        bool ok;
+        const int j = block_of(lst, it, nb, ok);
+        const uint32_t bar = smem_u32(&sm.v_full[st]);
+        mbar_arrive_expect_tx(bar, kTile);
+        tma_load_2d(smem_u32(sm.v[st]), &tmv, h * kD, j * kBN, bar);
+        tma_load_2d(smem_u32(sm.v[st]) + kHalf, &tmv, h * kD + 64, j * kBN, bar);
+        ++armed[st];
+      }
+      if (*abort) {
+        drain_wait(qbar, 0);
+        for (int s = 0; s < kStages; ++s)
+          if (armed[s]) drain_wait(smem_u32(&sm.v_full[s]), (armed[s] - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------------- MMA issuer
+    if (lane == 0 && cnt > 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, false, true);
+      const uint32_t qa = smem_u32(sm.q);
+      bool ok = mbar_wait(smem_u32(&sm.q_full), 0, abort, status);
+      for (int it = 0; ok && it <= cnt; ++it) {
+        if (it < cnt) {
+          const int st = it % kStages, b = it & 1;
+          if (!mbar_wait(smem_u32(&sm.k_full[st]), (it / kStages) & 1, abort, status)) break;
+          tc_fence_after();
+          const uint32_t ka = smem_u32(sm.k[st]);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            mma_ss(tmem + b * 128, smem_desc(qa + off, 16, 1024, kSwizzle128B),
+                   smem_desc(ka + off, 16, 1024, kSwizzle128B), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&sm.k_empty[st]));
+          tc_commit(smem_u32(&sm.s_full[b]));
+        }
+        if (it >= 1) {
+          const int t = it - 1, b = t & 1, st = t % kStages;
+          if (!mbar_wait(smem_u32(&sm.p_full[b]), (t >> 1) & 1, abort, status)) break;
+          if (!mbar_wait(smem_u32(&sm.v_full[st]), (t / kStages) & 1, abort, status)) break;
+          tc_fence_after();
+          const uint32_t va = smem_u32(sm.v[st]);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            mma_ts(tmem + 256, tmem + b * 128 + kk * 8, smem_desc(va + kk * 2048, kHalf, 1024, kSwizzle128B),
+                   idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&sm.v_empty[st]));
+          tc_commit(smem_u32(&sm.o_bar));
+        }
+      }
+      // all MMAs of this CTA have completed once this barrier flips
+      tc_commit(smem_u32(&sm.mma_done));
+      drain_wait(smem_u32(&sm.mma_done), 0);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax rows
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int it = 0; it < cnt; ++it) {
+      const int b = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[b]), (it >> 1) & 1, abort, status));
+      if (!ok) break;
+      tc_fence_after();
+      bool jok;
+      const int j = block_of(lst, it, nb, jok);
+      const int len = jok ? min(kBN, N - j * kBN) : 0;
+      if (!jok && r == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
+      float s[128];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t rr[32];
+        tmem_load_row32(lane_base + b * 128 + c4 * 32, rr);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) s[c4 * 32 + x] = __uint_as_float(rr[x]);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) mx = (c < len) ? fmaxf(mx, s[c]) : mx;
+      const float m_new = fmaxf(m_used, mx * kSl2);
+      if (m_new > m_used + kRescaleLog2) {
+        const float alpha = fast_exp2(m_used - m_new);
+        if (it > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_bar), (it - 1) & 1, abort, status));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t rr[32];
+            tmem_load_row32(lane_base + 256 + c4 * 32, rr);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) rr[x] = __float_as_uint(__uint_as_float(rr[x]) * alpha);
+            tmem_st32(lane_base + 256 + c4 * 32, rr);
+          }
+        }
+        l *= alpha;
+        m_used = m_new;
+      }
+      const bool live = m_used > -INFINITY;
+      float lsum = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          const int c = half * 64 + 2 * x;
+          const float p0 = (live && c < len) ? fast_exp2(fmaf(s[c], kSl2, -m_used)) : 0.f;
+          const float p1 = (live && c + 1 < len) ? fast_exp2(fmaf(s[c + 1], kSl2, -m_used)) : 0.f;
+          lsum += p0 + p1;
+          pk[x] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(lane_base + b * 128 + half * 32, pk);
+      }
+      tmem_wait_st();
+      l += lsum;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[b]));
+    }
+    // ---------------------------------------------------------------- epilogue
+    const int row = i * kBM + r;
+    __nv_bfloat16* orow = o + (int64_t)row * ld + (int64_t)h * kD;
+    if (ok && cnt > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_bar), (cnt - 1) & 1, abort, status));
+      if (ok) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t rr[32];
+          tmem_load_row32(lane_base + 256 + c4 * 32, rr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            pk[x] = pack_bf16x2(__uint_as_float(rr[2 * x]) * inv, __uint_as_float(rr[2 * x + 1]) * inv);
+          if (row < N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c4 * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+          }
+        }
+        if (row < N) lse[(size_t)h * N + row] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+      }
+    } else if (cnt == 0 && row < N) {
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) dst[x] = make_uint4(0u, 0u, 0u, 0u);
+      lse[(size_t)h * N + row] = -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------ layout self-test
+// One 128 x 128 x 128 tile: S = A B^T (both K-major, from shared memory) and
+// O = bf16(S) B (A from TMEM, B MN-major).  `variant` 1 swaps the two byte
+// offsets of the MN-major descriptor; every address stays inside the 96 KB
+// staging buffer either way.
+__global__ void __launch_bounds__(128, 1) umma_selftest_kernel(const __grid_constant__ CUtensorMap tma,
+                                                               const __grid_constant__ CUtensorMap tmb,
+                                                               float* __restrict__ out_s, float* __restrict__ out_o,
+                                                               int variant, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* a = base;
+  uint8_t* bt = base + kTile;
+  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar_ld), 1);
+    mbar_init(smem_u32(&bar_mma), 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(smem_u32(&bar_ld), 2 * kTile);
+    tma_load_2d(smem_u32(a), &tma, 0, 0, smem_u32(&bar_ld));
+    tma_load_2d(smem_u32(a) + kHalf, &tma, 64, 0, smem_u32(&bar_ld));
+    tma_load_2d(smem_u32(bt), &tmb, 0, 0, smem_u32(&bar_ld));
+    tma_load_2d(smem_u32(bt) + kHalf, &tmb, 64, 0, smem_u32(&bar_ld));
+  }
+  bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_ld), 0, &abort_flag, status));
+  __syncthreads();
+  if (threadIdx.x == 0 && ok) {
+    tc_fence_after();
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+      mma_ss(tmem, smem_desc(smem_u32(a) + off, 16, 1024, kSwizzle128B),
+             smem_desc(smem_u32(bt) + off, 16, 1024, kSwizzle128B), idesc_bf16_f32(128, 128, false, false),
+             kk > 0 ? 1u : 0u);
+    }
+    tc_commit(smem_u32(&bar_mma));
+  }
+  ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mma), 0, &abort_flag, status));
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  const int r = warp * 32 + lane;
+  if (ok) {
+    tc_fence_after();
+    for (int c4 = 0; c4 < 4; ++c4) {
+      uint32_t rr[32];
+      tmem_load_row32(lane_base + c4 * 32, rr);
+      for (int x = 0; x < 32; ++x) out_s[r * 128 + c4 * 32 + x] = __uint_as_float(rr[x]);
+      uint32_t pk[16];
+      for (int x = 0; x < 16; ++x) pk[x] = pack_bf16x2(__uint_as_float(rr[2 * x]), __uint_as_float(rr[2 * x + 1]));
+      uint32_t st32[32];
+      for (int x = 0; x < 32; ++x) st32[x] = 0;
+      // columns c4*16 .. c4*16+15 of the packed P
+      for (int x = 0; x < 16; ++x) st32[x] = pk[x];
+      asm volatile(
+          "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+          "%14, %15, %16};" ::"r"(lane_base + c4 * 16),
+          "r"(st32[0]), "r"(st32[1]), "r"(st32[2]), "r"(st32[3]), "r"(st32[4]), "r"(st32[5]), "r"(st32[6]),
+          "r"(st32[7]), "r"(st32[8]), "r"(st32[9]), "r"(st32[10]), "r"(st32[11]), "r"(st32[12]), "r"(st32[13]),
+          "r"(st32[14]), "r"(st32[15])
+          : "memory");
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && ok) {
+    tc_fence_after();
+    const uint32_t lbo = variant == 0 ? kHalf : 1024u, sbo = variant == 0 ? 1024u : kHalf;
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ts(tmem + 128, tmem + kk * 8, smem_desc(smem_u32(bt) + kk * 2048, lbo, sbo, kSwizzle128B),
+             idesc_bf16_f32(128, 128, false, true), kk > 0 ? 1u : 0u);
+    tc_commit(smem_u32(&bar_mma));
+  }
+  ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mma), 1, &abort_flag, status));
+  if (ok) {
+    tc_fence_after();
+    for (int c4 = 0; c4 < 4; ++c4) {
+      uint32_t rr[32];
+      tmem_load_row32(lane_base + 128 + c4 * 32, rr);
+      for (int x = 0; x < 32; ++x) out_o[r * 128 + c4 * 32 + x] = __uint_as_float(rr[x]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace
+
+cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
+                              const int32_t* counts, const int32_t* idx, int nb, void* o, float* lse,
+                              cudaStream_t st, uint32_t* status) {
+  CUtensorMap mq, mk, mv;
+  const uint64_t inner = (uint64_t)Hh * kD, row_bytes = (uint64_t)ld * 2;
+  if (!tensor_map_2d_bf16(&mq, q, inner, N, row_bytes, 64, kBM) ||
+      !tensor_map_2d_bf16(&mk, k, inner, N, row_bytes, 64, kBN) ||
+      !tensor_map_2d_bf16(&mv, v, inner, N, row_bytes, 64, kBN))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kFwdSmemBytes);
+  if (e != cudaSuccess) return e;
+  bsa_fwd_tc_kernel<<<(unsigned)Hh * nb, kThreads, kFwdSmemBytes, st>>>(
+      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, ld, N, counts, idx, nb, status);
+  return cudaGetLastError();
+}
+
+cudaError_t umma_selftest_launch(const void* a, const void* b, float* out_s, float* out_o, int variant,
+                                 cudaStream_t st, uint32_t* status) {
+  CUtensorMap ma, mb;
+  if (!tensor_map_2d_bf16(&ma, a, 128, 128, 256, 64, 128) || !tensor_map_2d_bf16(&mb, b, 128, 128, 256, 64, 128))
+    return cudaErrorInvalidValue;
+  const int smem = 3 * kTile + 1024;
+  cudaError_t e = cudaFuncSetAttribute(umma_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  umma_selftest_kernel<<<1, 128, smem, st>>>(ma, mb, out_s, out_o, variant, status);
+  return cudaGetLastError();
+}
+
+}  // namespace prism

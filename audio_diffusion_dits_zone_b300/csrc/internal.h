@@ -1,0 +1,70 @@
+// Host-side launchers shared between the C-ABI shim (prism_api.cu) and the kernel
+// files.  Arguments are validated by the shim before any launcher runs.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace prism {
+
+struct ZoneGeom {
+  int T, H, W;      // token grid
+  int zt, zh, zw;   // zone extents
+  int nzt, nzh, nzw;
+  int Z;            // zones
+  int max_tokens;   // tokens of the largest zone
+};
+
+struct ShapeSet {
+  int n;
+  int e[8][3];
+};
+
+// zone.cu
+size_t zone_ws_bytes(const ZoneGeom& g, int C, int dtype);
+cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const float* a2v, const ZoneGeom& g,
+                        const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm, void* ws, cudaStream_t st,
+                        uint32_t* status);
+
+// pool_score.cu
+cudaError_t pool_launch(const void* q, const void* k, const void* v, int dtype, int64_t ld, const int32_t* perm,
+                        int N, int Hh, int d, int B, void* qb, void* kb, void* vb, int64_t ldb, float* qbar,
+                        float* kbar, cudaStream_t st, uint32_t* status);
+cudaError_t scores_launch(const float* qbar, const float* kbar, int Hh, int nb, int d, float* scores,
+                          cudaStream_t st);
+
+// select.cu
+cudaError_t select_launch(const float* scores, int Hh, int nb, int k_top, float tau, int32_t* counts,
+                          int32_t* idx, cudaStream_t st);
+
+// bsa_simt.cu (CUDA-core attention for f32 inputs and shapes outside the tensor-core path)
+cudaError_t bsa_fwd_simt_launch(const void* q, const void* k, const void* v, int dtype, int64_t ld, int N, int Hh,
+                                int d, int B, const int32_t* counts, const int32_t* idx, int nb, void* o,
+                                float* lse, cudaStream_t st, uint32_t* status);
+cudaError_t bsa_bwd_simt_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                const float* lse, int dtype, int64_t ld, int N, int Hh, int d, int B,
+                                const int32_t* counts, const int32_t* idx, int nb, void* dq, void* dk, void* dv,
+                                const int32_t* tcounts, const int32_t* tidx, float* Drow, cudaStream_t st,
+                                uint32_t* status);
+
+// bsa_lists.cu (transposed kept lists and the backward row statistic)
+size_t lists_ws_bytes(int Hh, int nb);
+cudaError_t transpose_lists_launch(const int32_t* counts, const int32_t* idx, int Hh, int nb, void* ws,
+                                   int32_t** tcounts, int32_t** tidx, cudaStream_t st, uint32_t* status);
+cudaError_t row_dot_launch(const void* o, const void* dO, int dtype, int64_t ld, int N, int Hh, int d, float* Drow,
+                           cudaStream_t st);
+
+// bsa_tc_fwd.cu / bsa_tc_bwd.cu (tcgen05 tensor-core path: bf16, d = 128, B = 128)
+cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
+                              const int32_t* counts, const int32_t* idx, int nb, void* o, float* lse,
+                              cudaStream_t st, uint32_t* status);
+cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,
+                              const int32_t* idx, int nb, void* dq, void* dk, void* dv, const int32_t* tcounts,
+                              const int32_t* tidx, float* Drow, cudaStream_t st, uint32_t* status);
+
+// Driver entry point for tensor-map encoding (resolved once through the runtime).
+bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_outer);
+
+}  // namespace prism

@@ -1,0 +1,218 @@
+// Step 2 of the path: block-order gather, block-mean pooling of Q and K, and the
+// block score matrix.
+//
+// "Prism: dynamic sparse attention for 2K joint video-audio generation training",
+// section "Region-adapted block construction", paragraph 1: block-level features
+// are what the selection looks at.  Reading: the block mean of Q and of K (true
+// length for the short last block), score[h][i][j] = qbar[h][i] . kbar[h][j] / sqrt(d).
+//
+// pool_gather   one CTA per block: every thread owns 16-byte column vectors of the
+//               token rows and walks the block's rows, so each warp reads 512
+//               contiguous bytes per row (coalesced); it writes the block-order
+//               copies and the fp32 column sums.  HBM-bound: reads Q, K (, V) once.
+// scores        per head an [nb x d] x [d x nb] fp32 product on CUDA cores
+//               (64 x 64 output tile per CTA, 4 x 4 per thread).  fp32 keeps the
+//               block order the selection depends on close to the exact one.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace prism {
+namespace {
+
+constexpr int kPoolThreads = 256;
+
+template <typename T, int VW>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16, 8> {
+  using raw = uint4;
+  __device__ static void to_f32(const raw& r, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __bfloat1622float2(h[k]);
+      f[2 * k] = x.x;
+      f[2 * k + 1] = x.y;
+    }
+  }
+};
+template <>
+struct Vec<float, 4> {
+  using raw = uint4;
+  __device__ static void to_f32(const raw& r, float* f) {
+    const float* x = reinterpret_cast<const float*>(&r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) f[k] = x[k];
+  }
+};
+template <typename T>
+struct Vec<T, 1> {
+  using raw = T;
+  __device__ static void to_f32(const raw& r, float* f) { f[0] = prism::to_f32<T>(r); }
+};
+
+template <typename T, int VW>
+__global__ void __launch_bounds__(kPoolThreads)
+    pool_gather_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int64_t ld,
+                       const int32_t* __restrict__ perm, int N, int Hh, int d, int B, T* __restrict__ qb,
+                       T* __restrict__ kb, T* __restrict__ vb, int64_t ldb, float* __restrict__ qbar,
+                       float* __restrict__ kbar, int nb, uint32_t* status) {
+  using R = typename Vec<T, VW>::raw;
+  extern __shared__ int32_t rows[];  // source row of each block-order row
+  const int b = blockIdx.x;
+  const int r0 = b * B;
+  const int len = min(B, N - r0);
+  for (int r = threadIdx.x; r < len; r += kPoolThreads) {
+    int src = perm ? perm[r0 + r] : r0 + r;
+    if (src < 0 || src >= N) {  // a corrupt permutation is read as row 0 and flagged
+      flag_error(status, PRISM_DEV_BAD_INDEX);
+      src = 0;
+    }
+    rows[r] = src;
+  }
+  __syncthreads();
+  const int nvec = Hh * d / VW;
+  const float inv_len = 1.f / (float)len;
+  for (int vi = threadIdx.x; vi < nvec; vi += kPoolThreads) {
+    const int64_t col = (int64_t)vi * VW;
+    float aq[VW], ak[VW];
+#pragma unroll
+    for (int e = 0; e < VW; ++e) aq[e] = ak[e] = 0.f;
+    int r = 0;
+    for (; r + 4 <= len; r += 4) {
+      R xq[4], xk[4], xv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t src = (int64_t)rows[r + u] * ld + col;
+        xq[u] = *reinterpret_cast<const R*>(q + src);
+        xk[u] = *reinterpret_cast<const R*>(k + src);
+        if (vb) xv[u] = *reinterpret_cast<const R*>(v + src);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t dst = (int64_t)(r0 + r + u) * ldb + col;
+        if (qb) *reinterpret_cast<R*>(qb + dst) = xq[u];
+        if (kb) *reinterpret_cast<R*>(kb + dst) = xk[u];
+        if (vb) *reinterpret_cast<R*>(vb + dst) = xv[u];
+        float f[VW];
+        Vec<T, VW>::to_f32(xq[u], f);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) aq[e] += f[e];
+        Vec<T, VW>::to_f32(xk[u], f);
+#pragma unroll
+        for (int e = 0; e < VW; ++e) ak[e] += f[e];
+      }
+    }
+    for (; r < len; ++r) {
+      const int64_t src = (int64_t)rows[r] * ld + col;
+      const R xq = *reinterpret_cast<const R*>(q + src);
+      const R xk = *reinterpret_cast<const R*>(k + src);
+      const int64_t dst = (int64_t)(r0 + r) * ldb + col;
+      if (qb) *reinterpret_cast<R*>(qb + dst) = xq;
+      if (kb) *reinterpret_cast<R*>(kb + dst) = xk;
+      if (vb) *reinterpret_cast<R*>(vb + dst) = *reinterpret_cast<const R*>(v + src);
+      float f[VW];
+      Vec<T, VW>::to_f32(xq, f);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) aq[e] += f[e];
+      Vec<T, VW>::to_f32(xk, f);
+#pragma unroll
+      for (int e = 0; e < VW; ++e) ak[e] += f[e];
+    }
+    const int h = (int)(col / d), c = (int)(col - (int64_t)h * d);
+    const size_t o = ((size_t)h * nb + b) * d + c;
+#pragma unroll
+    for (int e = 0; e < VW; ++e) {
+      if (qbar) qbar[o + e] = aq[e] * inv_len;
+      if (kbar) kbar[o + e] = ak[e] * inv_len;
+    }
+  }
+}
+
+constexpr int kTile = 64, kKc = 32;
+
+__global__ void __launch_bounds__(256) scores_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar,
+                                                     int nb, int d, float scale, float* __restrict__ S) {
+  __shared__ float As[kKc][kTile + 4];
+  __shared__ float Bs[kKc][kTile + 4];
+  const int h = blockIdx.z;
+  const int i0 = blockIdx.y * kTile, j0 = blockIdx.x * kTile;
+  const float* A = qbar + (size_t)h * nb * d;
+  const float* Bm = kbar + (size_t)h * nb * d;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int c0 = 0; c0 < d; c0 += kKc) {
+    for (int e = threadIdx.x; e < kTile * kKc; e += 256) {
+      const int r = e / kKc, c = e - (e / kKc) * kKc;
+      const bool okc = c0 + c < d;
+      As[c][r] = (i0 + r < nb && okc) ? A[(size_t)(i0 + r) * d + c0 + c] : 0.f;
+      Bs[c][r] = (j0 + r < nb && okc) ? Bm[(size_t)(j0 + r) * d + c0 + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int c = 0; c < kKc; ++c) {
+      float a[4], bb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a[u] = As[c][ty + 16 * u];
+        bb[u] = Bs[c][tx + 16 * u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(a[u], bb[w], acc[u][w]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = i0 + ty + 16 * u;
+    if (i >= nb) continue;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int j = j0 + tx + 16 * w;
+      if (j < nb) S[((size_t)h * nb + i) * nb + j] = acc[u][w] * scale;
+    }
+  }
+}
+
+template <typename T, int VW>
+cudaError_t launch_pool(const void* q, const void* k, const void* v, int64_t ld, const int32_t* perm, int N, int Hh,
+                        int d, int B, void* qb, void* kb, void* vb, int64_t ldb, float* qbar, float* kbar,
+                        cudaStream_t st, uint32_t* status) {
+  const int nb = (N + B - 1) / B;
+  pool_gather_kernel<T, VW><<<nb, kPoolThreads, (size_t)B * sizeof(int32_t), st>>>(
+      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), ld, perm, N, Hh, d, B,
+      static_cast<T*>(qb), static_cast<T*>(kb), static_cast<T*>(vb), ldb, qbar, kbar, nb, status);
+  return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+cudaError_t pool_launch(const void* q, const void* k, const void* v, int dtype, int64_t ld, const int32_t* perm,
+                        int N, int Hh, int d, int B, void* qb, void* kb, void* vb, int64_t ldb, float* qbar,
+                        float* kbar, cudaStream_t st, uint32_t* status) {
+  const bool ptr_ok = aligned16(q) && aligned16(k) && (!v || aligned16(v)) && (!qb || aligned16(qb)) &&
+                      (!kb || aligned16(kb)) && (!vb || aligned16(vb));
+  if (dtype == PRISM_BF16) {
+    if (ptr_ok && d % 8 == 0 && ld % 8 == 0 && ldb % 8 == 0)
+      return launch_pool<__nv_bfloat16, 8>(q, k, v, ld, perm, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
+    return launch_pool<__nv_bfloat16, 1>(q, k, v, ld, perm, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
+  }
+  if (ptr_ok && d % 4 == 0 && ld % 4 == 0 && ldb % 4 == 0)
+    return launch_pool<float, 4>(q, k, v, ld, perm, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
+  return launch_pool<float, 1>(q, k, v, ld, perm, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
+}
+
+cudaError_t scores_launch(const float* qbar, const float* kbar, int Hh, int nb, int d, float* scores,
+                          cudaStream_t st) {
+  const dim3 grid((nb + kTile - 1) / kTile, (nb + kTile - 1) / kTile, Hh);
+  scores_kernel<<<grid, 256, 0, st>>>(qbar, kbar, nb, d, 1.0f / sqrtf((float)d), scores);
+  return cudaGetLastError();
+}
+
+}  // namespace prism

@@ -1,0 +1,253 @@
+// C ABI of libprism.so (declared in include/prism.h): argument checks, workspace
+// sizing, dispatch to the kernel launchers, and the device status word.
+//
+// Nothing here allocates device memory: scratch space is the caller's workspace.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace prism {
+cudaError_t umma_selftest_launch(const void* a, const void* b, float* out_s, float* out_o, int variant,
+                                 cudaStream_t st, uint32_t* status);
+}
+
+namespace {
+
+__device__ uint32_t g_status_word;
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return PRISM_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PRISM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device address of the status word of the current device, resolved once per device.
+uint32_t* status_ptr() {
+  static std::mutex mu;
+  static uint32_t* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+constexpr size_t kMinWs = 256;
+
+size_t ws_round(size_t x) { return x < kMinWs ? kMinWs : ((x + 255) & ~(size_t)255); }
+
+// Common workspace protocol: ws == NULL -> report the size; else check it.
+bool ws_query(void* ws, size_t* ws_bytes, size_t need, int* rc) {
+  if (!ws_bytes) {
+    *rc = fail(PRISM_EINVAL, "ws_bytes must not be NULL");
+    return true;
+  }
+  if (!ws) {
+    *ws_bytes = need;
+    *rc = ok();
+    return true;
+  }
+  if (*ws_bytes < need) {
+    *rc = fail(PRISM_EINVAL, "workspace of %zu bytes is smaller than the %zu required", *ws_bytes, need);
+    return true;
+  }
+  if (reinterpret_cast<uintptr_t>(ws) & 255) {
+    *rc = fail(PRISM_EINVAL, "workspace must be 256-byte aligned");
+    return true;
+  }
+  return false;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int check_attention_args(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld, int32_t N,
+                         int32_t Hh, int32_t d, int32_t B, const int32_t* counts, const int32_t* idx, int32_t nb) {
+  if (dtype != PRISM_F32 && dtype != PRISM_BF16) return fail(PRISM_EINVAL, "dtype must be PRISM_F32 or PRISM_BF16");
+  if (N < 1 || Hh < 1) return fail(PRISM_EINVAL, "N and Hh must be >= 1 (got %d, %d)", N, Hh);
+  if (d != 64 && d != 128) return fail(PRISM_EUNSUPPORTED, "head dim %d not built (64 or 128)", d);
+  if (B != 64 && B != 128) return fail(PRISM_EUNSUPPORTED, "block size %d not built (64 or 128)", B);
+  if (nb != cdiv(N, B)) return fail(PRISM_EINVAL, "nb = %d but ceil(N / B) = %lld", nb, (long long)cdiv(N, B));
+  if (ld < (int64_t)Hh * d) return fail(PRISM_EINVAL, "ld = %lld < Hh * d = %d", (long long)ld, Hh * d);
+  if (!q || !k || !v || !counts || !idx) return fail(PRISM_EINVAL, "NULL input pointer");
+  if ((int64_t)Hh * nb * nb > ((int64_t)1 << 40)) return fail(PRISM_EINVAL, "Hh * nb * nb too large");
+  return PRISM_OK;
+}
+
+bool use_tc(int32_t dtype, int32_t d, int32_t B, int64_t ld, std::initializer_list<const void*> ptrs) {
+  if (dtype != PRISM_BF16 || d != 128 || B != 128 || ld % 8 != 0) return false;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int prism_zone_shapes(const void* feat, int32_t feat_dtype, int64_t feat_ld, int32_t C, const float* a2v, int32_t T,
+                      int32_t H, int32_t W, int32_t zt, int32_t zh, int32_t zw, const int32_t* shapes,
+                      int32_t n_shapes, int32_t* zone_shape, int32_t* perm, void* ws, size_t* ws_bytes,
+                      void* stream) {
+  if (feat_dtype != PRISM_F32 && feat_dtype != PRISM_BF16) return fail(PRISM_EINVAL, "feat_dtype invalid");
+  if (T < 1 || H < 1 || W < 1) return fail(PRISM_EINVAL, "grid must be positive");
+  if ((int64_t)T * H * W > INT32_MAX) return fail(PRISM_EINVAL, "too many tokens");
+  if (zt < 1 || zh < 1 || zw < 1) return fail(PRISM_EINVAL, "zone extents must be >= 1");
+  if (C < 1 || feat_ld < C) return fail(PRISM_EINVAL, "need 1 <= C <= feat_ld");
+  if (n_shapes < 1 || n_shapes > 8 || !shapes) return fail(PRISM_EINVAL, "need 1..8 shapes (host array)");
+  prism::ShapeSet ss{};
+  ss.n = n_shapes;
+  for (int s = 0; s < n_shapes; ++s)
+    for (int a = 0; a < 3; ++a) {
+      ss.e[s][a] = shapes[3 * s + a];
+      if (ss.e[s][a] < 1) return fail(PRISM_EINVAL, "shape extents must be >= 1");
+    }
+  prism::ZoneGeom g{};
+  g.T = T, g.H = H, g.W = W, g.zt = zt, g.zh = zh, g.zw = zw;
+  g.nzt = (int)cdiv(T, zt), g.nzh = (int)cdiv(H, zh), g.nzw = (int)cdiv(W, zw);
+  g.Z = g.nzt * g.nzh * g.nzw;
+  g.max_tokens = std::min(zt, T) * std::min(zh, H) * std::min(zw, W);
+  if ((int64_t)g.max_tokens * 8 * 4 > 200 * 1024)
+    return fail(PRISM_EUNSUPPORTED, "zones of %d tokens exceed the shared-memory staging limit (6400)",
+                g.max_tokens);
+  int rc;
+  if (ws_query(ws, ws_bytes, ws_round(prism::zone_ws_bytes(g, C, feat_dtype)), &rc)) return rc;
+  if (!feat || !a2v || !zone_shape || !perm) return fail(PRISM_EINVAL, "NULL pointer");
+  cudaError_t e = prism::zone_launch(feat, feat_dtype, feat_ld, C, a2v, g, ss, zone_shape, perm, ws,
+                                     static_cast<cudaStream_t>(stream), status_ptr());
+  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_zone_shapes");
+}
+
+int prism_pool_score(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld, const int32_t* perm,
+                     int32_t N, int32_t Hh, int32_t d, int32_t B, void* q_blk, void* k_blk, void* v_blk,
+                     int64_t ld_blk, float* qbar, float* kbar, float* scores, void* stream) {
+  if (dtype != PRISM_F32 && dtype != PRISM_BF16) return fail(PRISM_EINVAL, "dtype invalid");
+  if (N < 1 || Hh < 1 || d < 1 || B < 1) return fail(PRISM_EINVAL, "sizes must be >= 1");
+  if (d > 256) return fail(PRISM_EUNSUPPORTED, "d > 256");
+  if (!q || !k) return fail(PRISM_EINVAL, "q and k must not be NULL");
+  if (ld < (int64_t)Hh * d) return fail(PRISM_EINVAL, "ld < Hh * d");
+  const bool copies = q_blk || k_blk || v_blk;
+  if (!perm && copies) return fail(PRISM_EINVAL, "block-order copies need perm");
+  if (copies && ld_blk < (int64_t)Hh * d) return fail(PRISM_EINVAL, "ld_blk < Hh * d");
+  if (v_blk && !v) return fail(PRISM_EINVAL, "v_blk needs v");
+  if (scores && (!qbar || !kbar)) return fail(PRISM_EINVAL, "scores need the qbar and kbar buffers");
+  const int nb = (int)cdiv(N, B);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (qbar || kbar || copies)
+    e = prism::pool_launch(q, k, v, dtype, ld, perm, N, Hh, d, B, q_blk, k_blk, v_blk, copies ? ld_blk : ld, qbar,
+                           kbar, st, status_ptr());
+  if (e == cudaSuccess && scores) e = prism::scores_launch(qbar, kbar, Hh, nb, d, scores, st);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_pool_score");
+}
+
+int prism_select(const float* scores, int32_t Hh, int32_t nb, double sparsity, double cdf_tau, int32_t* counts,
+                 int32_t* idx, void* stream) {
+  if (!scores || !counts || !idx) return fail(PRISM_EINVAL, "NULL pointer");
+  if (Hh < 1 || nb < 1) return fail(PRISM_EINVAL, "Hh and nb must be >= 1");
+  if (nb > 4096) return fail(PRISM_EUNSUPPORTED, "nb = %d > 4096", nb);
+  if (!(sparsity >= 0.0 && sparsity < 1.0)) return fail(PRISM_EINVAL, "sparsity must be in [0, 1)");
+  if (!(cdf_tau >= 0.0 && cdf_tau <= 1.0)) return fail(PRISM_EINVAL, "cdf_tau must be in [0, 1]");
+  const double kk = std::ceil((1.0 - sparsity) * nb - 1e-9);
+  const int k_top = (int)std::min<double>(nb, std::max<double>(1.0, kk));
+  cudaError_t e = prism::select_launch(scores, Hh, nb, k_top, (float)cdf_tau, counts, idx,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_select");
+}
+
+int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32_t dtype, int64_t ld, int32_t N,
+                  int32_t Hh, int32_t d, int32_t B, const int32_t* counts, const int32_t* idx, int32_t nb,
+                  void* o_blk, float* lse, void* ws, size_t* ws_bytes, void* stream) {
+  int rc = check_attention_args(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb);
+  if (rc != PRISM_OK) return rc;
+  if (ws_query(ws, ws_bytes, ws_round(0), &rc)) return rc;
+  if (!o_blk || !lse) return fail(PRISM_EINVAL, "NULL output pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (use_tc(dtype, d, B, ld, {q_blk, k_blk, v_blk, o_blk}))
+    e = prism::bsa_fwd_tc_launch(q_blk, k_blk, v_blk, ld, N, Hh, counts, idx, nb, o_blk, lse, st, status_ptr());
+  else
+    e = prism::bsa_fwd_simt_launch(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb, o_blk, lse, st,
+                                   status_ptr());
+  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_bsa_fwd");
+}
+
+int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk, const void* o_blk, const void* do_blk,
+                  const float* lse, int32_t dtype, int64_t ld, int32_t N, int32_t Hh, int32_t d, int32_t B,
+                  const int32_t* counts, const int32_t* idx, int32_t nb, void* dq, void* dk, void* dv, void* ws,
+                  size_t* ws_bytes, void* stream) {
+  int rc = check_attention_args(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb);
+  if (rc != PRISM_OK) return rc;
+  const size_t lists = prism::lists_ws_bytes(Hh, nb);
+  const size_t drow = ((size_t)Hh * N * sizeof(float) + 255) & ~(size_t)255;
+  if (ws_query(ws, ws_bytes, ws_round(lists + drow), &rc)) return rc;
+  if (!o_blk || !do_blk || !lse || !dq || !dk || !dv) return fail(PRISM_EINVAL, "NULL pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* tcounts = nullptr;
+  int32_t* tidx = nullptr;
+  float* Drow = reinterpret_cast<float*>(static_cast<char*>(ws) + lists);
+  cudaError_t e = prism::transpose_lists_launch(counts, idx, Hh, nb, ws, &tcounts, &tidx, st, status_ptr());
+  if (e == cudaSuccess)
+    e = prism::bsa_bwd_simt_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, dtype, ld, N, Hh, d, B, counts, idx,
+                                   nb, dq, dk, dv, tcounts, tidx, Drow, st, status_ptr());
+  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_bsa_bwd");
+}
+
+int prism_status_check(void* stream, uint32_t* word) {
+  uint32_t* p = status_ptr();
+  if (!p) return fail(PRISM_ECUDA, "no CUDA device");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t w = 0;
+  cudaError_t e = cudaMemcpyAsync(&w, p, sizeof(w), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "prism_status_check");
+  if (word) *word = w;
+  if (w & PRISM_DEV_TIMEOUT) return fail(PRISM_ETIMEOUT, "a bounded device wait gave up (status 0x%x)", w);
+  if (w & PRISM_DEV_BAD_INDEX) return fail(PRISM_EINDEX, "an out-of-range block index was skipped (status 0x%x)", w);
+  if (w) return fail(PRISM_ECUDA, "device status 0x%x", w);
+  return ok();
+}
+
+const char* prism_last_error(void) { return g_last_error.c_str(); }
+
+const char* prism_build_info(void) {
+  return "libprism 0.1 | sm_103a | bsa_fwd: tcgen05+TMA for bf16 d=128 B=128, CUDA cores otherwise | "
+         "bsa_bwd: CUDA cores | select: nb <= 4096 | zone: <= 6400 tokens per zone";
+}
+
+int prism_selftest_umma(const void* a, const void* b, float* out_s, float* out_o, int32_t variant, void* stream) {
+  if (!a || !b || !out_s || !out_o || !aligned16(a) || !aligned16(b)) return fail(PRISM_EINVAL, "bad pointer");
+  cudaError_t e = prism::umma_selftest_launch(a, b, out_s, out_o, variant ? 1 : 0, static_cast<cudaStream_t>(stream),
+                                              status_ptr());
+  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_selftest_umma");
+}
+
+}  // extern "C"

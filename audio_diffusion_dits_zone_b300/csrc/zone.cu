@@ -1,0 +1,352 @@
+// Step 1 of the path: per-macro-zone block shape and the block-order permutation.
+//
+// "Prism: dynamic sparse attention for 2K joint video-audio generation training",
+// section "Region-adapted block construction", paragraph 1: per macro-zone, the
+// channel-wise variance of the video features (how fast, and along which axis,
+// the content changes) and the audio-to-video cross-attention feature norm (how
+// strongly audio drives the region) decide the block shape; axes of fast change or
+// strong coupling are split more finely.
+//
+// Readings (the page gives no formula): v_a = mean over channels and over the
+// zone's lines along axis a of the population variance along the line; u_a = the
+// same for the A2V field; w = zone mean A2V / largest zone mean;
+// S_a = v_a / sum v + w u_a / sum u; shape = argmin sum_a S_a log2 e_a (first on
+// ties).  Block order: zones raster, tiles of the zone's shape in tile-raster order
+// clipped at the zone edge, tokens raster inside a tile.
+//
+// Kernels (all HBM-bound or tiny):
+//   zone_partial   one CTA per (zone, channel chunk): the chunk of the zone is
+//                  staged in shared memory (coalesced 16-byte loads) and the
+//                  two-pass line variances are summed for the three axes;
+//   zone_finalize  one CTA per zone: fixed-order sum over chunks, A2V statistics;
+//   zone_choose    one CTA: largest zone mean, per-zone scores, fp32 costs, argmin;
+//   zone_perm      one thread per token: closed-form block-order position.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace prism {
+namespace {
+
+constexpr int kZoneThreads = 256;
+constexpr int kSmemBudget = 200 * 1024;
+
+struct ZoneBox {
+  int t0, h0, w0, Lt, Lh, Lw;
+};
+
+__device__ __forceinline__ ZoneBox zone_box(const ZoneGeom& g, int z) {
+  ZoneBox b;
+  const int zt = z / (g.nzh * g.nzw);
+  const int rem = z - zt * g.nzh * g.nzw;
+  const int zh = rem / g.nzw;
+  const int zw = rem - zh * g.nzw;
+  b.t0 = zt * g.zt;
+  b.h0 = zh * g.zh;
+  b.w0 = zw * g.zw;
+  b.Lt = min(g.zt, g.T - b.t0);
+  b.Lh = min(g.zh, g.H - b.h0);
+  b.Lw = min(g.zw, g.W - b.w0);
+  return b;
+}
+
+// Line geometry for axis a of a zone: number of lines, line length, first token
+// of line `line` and the token stride along the line (local token p = (lt*Lh+lh)*Lw+lw).
+__device__ __forceinline__ void line_of(const ZoneBox& b, int a, int line, int& p0, int& sp) {
+  if (a == 0) {
+    const int lh = line / b.Lw, lw = line - (line / b.Lw) * b.Lw;
+    p0 = lh * b.Lw + lw;
+    sp = b.Lh * b.Lw;
+  } else if (a == 1) {
+    const int lt = line / b.Lw, lw = line - (line / b.Lw) * b.Lw;
+    p0 = lt * b.Lh * b.Lw + lw;
+    sp = b.Lw;
+  } else {
+    const int lt = line / b.Lh, lh = line - (line / b.Lh) * b.Lh;
+    p0 = (lt * b.Lh + lh) * b.Lw;
+    sp = 1;
+  }
+}
+__device__ __forceinline__ int nlines_of(const ZoneBox& b, int a) {
+  return a == 0 ? b.Lh * b.Lw : (a == 1 ? b.Lt * b.Lw : b.Lt * b.Lh);
+}
+__device__ __forceinline__ int len_of(const ZoneBox& b, int a) { return a == 0 ? b.Lt : (a == 1 ? b.Lh : b.Lw); }
+
+// Block-wide sums of three values; every thread receives the three totals.
+// red must hold NW * 3 + 3 floats.  Fixed reduction order (deterministic).
+template <int NW>
+__device__ __forceinline__ void block_sum3(float (&acc)[3], float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    float v = acc[a];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[warp * 3 + a] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < 3) {
+    float s = 0.f;
+    for (int w = 0; w < NW; ++w) s += red[w * 3 + threadIdx.x];
+    red[NW * 3 + threadIdx.x] = s;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int a = 0; a < 3; ++a) acc[a] = red[NW * 3 + a];
+  __syncthreads();
+}
+
+// Sum over the chunk's channels and the zone's lines of sum_x (x - line mean)^2,
+// for each axis.  part[(z * nchunks + chunk) * 3 + a].
+template <typename T, int VW>
+__global__ void __launch_bounds__(kZoneThreads) zone_partial_kernel(const T* __restrict__ feat, int64_t ld, int C,
+                                                                    ZoneGeom g, int CH, float* __restrict__ part) {
+  extern __shared__ __align__(16) float xs[];  // [tokens][CH] fp32
+  __shared__ float red[(kZoneThreads / 32) * 3 + 3];
+  const int z = blockIdx.x, chunk = blockIdx.y, nchunks = gridDim.y;
+  const int c0 = chunk * CH;
+  const ZoneBox b = zone_box(g, z);
+  const int ntok = b.Lt * b.Lh * b.Lw;
+  const int nch = min(CH, C - c0);
+
+  if (VW > 1 && nch == CH) {
+    const int vpr = CH / VW;  // vectors per token row
+    for (int e = threadIdx.x; e < ntok * vpr; e += kZoneThreads) {
+      const int p = e / vpr, q = e - (e / vpr) * vpr;
+      const int lt = p / (b.Lh * b.Lw), rem = p - lt * b.Lh * b.Lw, lh = rem / b.Lw, lw = rem - lh * b.Lw;
+      const int64_t n = ((int64_t)(b.t0 + lt) * g.H + (b.h0 + lh)) * g.W + (b.w0 + lw);
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(feat + n * ld + c0 + q * VW));
+      float* dst = xs + p * CH + q * VW;
+      if constexpr (sizeof(T) == 2) {
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(h2[k]);
+          dst[2 * k] = f.x;
+          dst[2 * k + 1] = f.y;
+        }
+      } else {
+        const float* f = reinterpret_cast<const float*>(&raw);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = f[k];
+      }
+    }
+  } else {
+    for (int e = threadIdx.x; e < ntok * CH; e += kZoneThreads) {
+      const int p = e / CH, c = e - (e / CH) * CH;
+      const int lt = p / (b.Lh * b.Lw), rem = p - lt * b.Lh * b.Lw, lh = rem / b.Lw, lw = rem - lh * b.Lw;
+      const int64_t n = ((int64_t)(b.t0 + lt) * g.H + (b.h0 + lh)) * g.W + (b.w0 + lw);
+      xs[p * CH + c] = c < nch ? to_f32<T>(feat[n * ld + c0 + c]) : 0.f;
+    }
+  }
+  __syncthreads();
+
+  float acc[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    const int L = len_of(b, a);
+    if (L < 2) continue;
+    const float inv_L = 1.f / (float)L;
+    const int items = nlines_of(b, a) * CH;
+    for (int e = threadIdx.x; e < items; e += kZoneThreads) {
+      const int line = e / CH, c = e - (e / CH) * CH;
+      int p0, sp;
+      line_of(b, a, line, p0, sp);
+      const float* x = xs + p0 * CH + c;
+      float s = 0.f;
+      for (int k = 0; k < L; ++k) s += x[k * sp * CH];
+      const float mu = s * inv_L;
+      float ss = 0.f;
+      for (int k = 0; k < L; ++k) {
+        const float dlt = x[k * sp * CH] - mu;
+        ss = fmaf(dlt, dlt, ss);
+      }
+      acc[a] += ss;
+    }
+  }
+  block_sum3<kZoneThreads / 32>(acc, red);
+  if (threadIdx.x < 3) part[((size_t)z * nchunks + chunk) * 3 + threadIdx.x] = acc[threadIdx.x];
+}
+
+// stats[z * 8 + {0,1,2}] = v_a, {3,4,5} = u_a, 6 = zone mean of a2v.
+__global__ void __launch_bounds__(kZoneThreads) zone_finalize_kernel(const float* __restrict__ part, int nchunks,
+                                                                     const float* __restrict__ a2v, ZoneGeom g,
+                                                                     int C, float* __restrict__ stats) {
+  extern __shared__ float as[];  // zone's a2v values
+  __shared__ float red[(kZoneThreads / 32) * 3 + 3];
+  const int z = blockIdx.x;
+  const ZoneBox b = zone_box(g, z);
+  const int ntok = b.Lt * b.Lh * b.Lw;
+  for (int p = threadIdx.x; p < ntok; p += kZoneThreads) {
+    const int lt = p / (b.Lh * b.Lw), rem = p - lt * b.Lh * b.Lw, lh = rem / b.Lw, lw = rem - lh * b.Lw;
+    as[p] = a2v[((int64_t)(b.t0 + lt) * g.H + (b.h0 + lh)) * g.W + (b.w0 + lw)];
+  }
+  __syncthreads();
+  float acc[3] = {0.f, 0.f, 0.f};
+  for (int a = 0; a < 3; ++a) {
+    const int L = len_of(b, a);
+    if (L < 2) continue;
+    const float inv_L = 1.f / (float)L;
+    for (int line = threadIdx.x; line < nlines_of(b, a); line += kZoneThreads) {
+      int p0, sp;
+      line_of(b, a, line, p0, sp);
+      float s = 0.f;
+      for (int k = 0; k < L; ++k) s += as[p0 + k * sp];
+      const float mu = s * inv_L;
+      float ss = 0.f;
+      for (int k = 0; k < L; ++k) {
+        const float dlt = as[p0 + k * sp] - mu;
+        ss = fmaf(dlt, dlt, ss);
+      }
+      acc[a] += ss;
+    }
+  }
+  block_sum3<kZoneThreads / 32>(acc, red);
+  float u[3] = {acc[0], acc[1], acc[2]};
+  float m[3] = {0.f, 0.f, 0.f};
+  for (int p = threadIdx.x; p < ntok; p += kZoneThreads) m[0] += as[p];
+  block_sum3<kZoneThreads / 32>(m, red);
+  if (threadIdx.x == 0) {
+    const float inv_tok = 1.f / (float)ntok;
+    for (int a = 0; a < 3; ++a) {
+      float s = 0.f;
+      for (int c = 0; c < nchunks; ++c) s += part[((size_t)z * nchunks + c) * 3 + a];
+      stats[z * 8 + a] = s / ((float)C * (float)ntok);
+      stats[z * 8 + 3 + a] = u[a] * inv_tok;
+    }
+    stats[z * 8 + 6] = m[0] * inv_tok;
+    stats[z * 8 + 7] = 0.f;
+  }
+}
+
+__global__ void __launch_bounds__(1024) zone_choose_kernel(const float* __restrict__ stats, int Z, ShapeSet shapes,
+                                                           int32_t* __restrict__ zone_shape) {
+  __shared__ float red[32];
+  float mx = 0.f;
+  for (int z = threadIdx.x; z < Z; z += blockDim.x) mx = fmaxf(mx, stats[z * 8 + 6]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    red[0] = m;
+  }
+  __syncthreads();
+  const float amax = red[0];
+  float lg[8][3];
+  for (int s = 0; s < shapes.n; ++s)
+    for (int a = 0; a < 3; ++a) lg[s][a] = log2f((float)shapes.e[s][a]);
+  for (int z = threadIdx.x; z < Z; z += blockDim.x) {
+    const float* st = stats + z * 8;
+    const float vs = st[0] + st[1] + st[2];
+    const float us = st[3] + st[4] + st[5];
+    const float w = amax > 0.f ? st[6] / amax : 0.f;
+    float S[3];
+    for (int a = 0; a < 3; ++a) S[a] = (vs > 0.f ? st[a] / vs : 0.f) + w * (us > 0.f ? st[3 + a] / us : 0.f);
+    int best = 0;
+    float bc = 0.f;
+    for (int s = 0; s < shapes.n; ++s) {
+      const float c = S[0] * lg[s][0] + S[1] * lg[s][1] + S[2] * lg[s][2];
+      if (s == 0 || c < bc) {
+        bc = c;
+        best = s;
+      }
+    }
+    zone_shape[z] = best;
+  }
+}
+
+__global__ void zone_perm_kernel(ZoneGeom g, const int32_t* __restrict__ zone_shape, ShapeSet shapes,
+                                 int32_t* __restrict__ perm) {
+  const int64_t N = (int64_t)g.T * g.H * g.W;
+  for (int64_t n = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; n < N; n += (int64_t)gridDim.x * blockDim.x) {
+    const int w = (int)(n % g.W);
+    const int h = (int)((n / g.W) % g.H);
+    const int t = (int)(n / ((int64_t)g.W * g.H));
+    const int zi_t = t / g.zt, zi_h = h / g.zh, zi_w = w / g.zw;
+    const int z = (zi_t * g.nzh + zi_h) * g.nzw + zi_w;
+    const int Lt = min(g.zt, g.T - zi_t * g.zt), Lh = min(g.zh, g.H - zi_h * g.zh), Lw = min(g.zw, g.W - zi_w * g.zw);
+    // tokens of all zones before z in raster order (clipping is separable per axis)
+    const int64_t zone_off = (int64_t)zi_t * g.zt * g.H * g.W + (int64_t)Lt * zi_h * g.zh * g.W +
+                             (int64_t)Lt * Lh * zi_w * g.zw;
+    const int s = zone_shape[z];
+    const int et = shapes.e[s][0], eh = shapes.e[s][1], ew = shapes.e[s][2];
+    const int lt = t - zi_t * g.zt, lh = h - zi_h * g.zh, lw = w - zi_w * g.zw;
+    const int tt = lt / et, th = lh / eh, tw = lw / ew;
+    const int Et = min(et, Lt - tt * et), Eh = min(eh, Lh - th * eh), Ew = min(ew, Lw - tw * ew);
+    const int64_t tile_off = (int64_t)tt * et * Lh * Lw + (int64_t)Et * th * eh * Lw + (int64_t)Et * Eh * tw * ew;
+    const int within = ((lt - tt * et) * Eh + (lh - th * eh)) * Ew + (lw - tw * ew);
+    perm[zone_off + tile_off + within] = (int32_t)n;
+  }
+}
+
+int chunk_channels(const ZoneGeom& g) {
+  for (int ch = 64; ch >= 8; ch >>= 1)
+    if ((size_t)g.max_tokens * ch * sizeof(float) <= (size_t)kSmemBudget) return ch;
+  return 0;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+size_t zone_ws_bytes(const ZoneGeom& g, int C, int /*dtype*/) {
+  const int ch = chunk_channels(g);
+  if (ch == 0) return 0;
+  const int nchunks = (C + ch - 1) / ch;
+  return align256((size_t)g.Z * nchunks * 3 * sizeof(float)) + align256((size_t)g.Z * 8 * sizeof(float));
+}
+
+cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const float* a2v, const ZoneGeom& g,
+                        const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm, void* ws, cudaStream_t st,
+                        uint32_t* /*status*/) {
+  const int ch = chunk_channels(g);
+  const int nchunks = (C + ch - 1) / ch;
+  float* part = reinterpret_cast<float*>(ws);
+  float* stats = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)g.Z * nchunks * 3 * 4));
+  const size_t smem = (size_t)g.max_tokens * ch * sizeof(float);
+  const dim3 grid(g.Z, nchunks);
+  cudaError_t e;
+  if (dtype == PRISM_BF16) {
+    const bool vec = (ld % 8 == 0) && (C % 8 == 0) && ((reinterpret_cast<uintptr_t>(feat) & 15) == 0);
+    if (vec) {
+      auto k = zone_partial_kernel<__nv_bfloat16, 8>;
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+      k<<<grid, kZoneThreads, smem, st>>>(static_cast<const __nv_bfloat16*>(feat), ld, C, g, ch, part);
+    } else {
+      auto k = zone_partial_kernel<__nv_bfloat16, 1>;
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+      k<<<grid, kZoneThreads, smem, st>>>(static_cast<const __nv_bfloat16*>(feat), ld, C, g, ch, part);
+    }
+  } else {
+    const bool vec = (ld % 4 == 0) && (C % 4 == 0) && ((reinterpret_cast<uintptr_t>(feat) & 15) == 0);
+    if (vec) {
+      auto k = zone_partial_kernel<float, 4>;
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+      k<<<grid, kZoneThreads, smem, st>>>(static_cast<const float*>(feat), ld, C, g, ch, part);
+    } else {
+      auto k = zone_partial_kernel<float, 1>;
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+      k<<<grid, kZoneThreads, smem, st>>>(static_cast<const float*>(feat), ld, C, g, ch, part);
+    }
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  zone_finalize_kernel<<<g.Z, kZoneThreads, (size_t)g.max_tokens * sizeof(float), st>>>(part, nchunks, a2v, g, C,
+                                                                                        stats);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  zone_choose_kernel<<<1, 1024, 0, st>>>(stats, g.Z, shapes, zone_shape);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t N = (int64_t)g.T * g.H * g.W;
+  const int blocks = (int)std::min<int64_t>((N + 255) / 256, 148 * 16);
+  zone_perm_kernel<<<blocks, 256, 0, st>>>(g, zone_shape, shapes, perm);
+  return cudaGetLastError();
+}
+
+}  // namespace prism

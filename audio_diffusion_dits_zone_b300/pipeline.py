@@ -1,0 +1,127 @@
+"""One Prism attention layer on the device: buffers for a workload and the calls of
+the path in order (zone shapes -> pool + score -> select -> attention forward ->
+backward).  PyTorch only provides the memory and the stream; every step is a
+libprism call.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import prism as P
+from . import synth
+
+
+class PrismLayer:
+    """Device-resident state of one attention layer for a ``synth.Workload``."""
+
+    def __init__(self, wl: synth.Workload, device="cuda", sparsity=None, train=None):
+        self.wl = wl
+        self.device = torch.device(device)
+        self.sparsity = wl.sparsity if sparsity is None else sparsity
+        self.train = (wl.mode == "fwd+bwd") if train is None else train
+        N, Hh, d, nb = wl.N, wl.heads, wl.d, wl.nb
+        dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+        self.dtype = dt
+        e = dict(device=self.device)
+        T, H, W = wl.grid
+        self.Z = -(-T // wl.zone[0]) * -(-H // wl.zone[1]) * -(-W // wl.zone[2])
+        self.q = torch.empty(N, Hh, d, dtype=dt, **e)
+        self.k = torch.empty(N, Hh, d, dtype=dt, **e)
+        self.v = torch.empty(N, Hh, d, dtype=dt, **e)
+        self.a2v = torch.empty(N, dtype=torch.float32, **e)
+        self.zone_shape = torch.empty(self.Z, dtype=torch.int32, **e)
+        self.perm = torch.empty(N, dtype=torch.int32, **e)
+        self.q_blk = torch.empty_like(self.q)
+        self.k_blk = torch.empty_like(self.k)
+        self.v_blk = torch.empty_like(self.v)
+        self.qbar = torch.empty(Hh, nb, d, dtype=torch.float32, **e)
+        self.kbar = torch.empty(Hh, nb, d, dtype=torch.float32, **e)
+        self.scores = torch.empty(Hh, nb, nb, dtype=torch.float32, **e)
+        self.counts = torch.empty(Hh, nb, dtype=torch.int32, **e)
+        self.idx = torch.empty(Hh, nb, nb, dtype=torch.int32, **e)
+        self.o_blk = torch.empty_like(self.q)
+        self.lse = torch.empty(Hh, N, dtype=torch.float32, **e)
+        self.ws_zone = self.ws_fwd = self.ws_bwd = None
+        if self.train:
+            self.do_blk = torch.empty_like(self.q)
+            self.dq = torch.empty_like(self.q)
+            self.dk = torch.empty_like(self.q)
+            self.dv = torch.empty_like(self.q)
+
+    # ------------------------------------------------------------------ inputs
+    def load_inputs(self, threads=8):
+        """Generate the seeded inputs on the host and copy them into the device buffers."""
+        wl = self.wl
+        heads = list(range(wl.heads))
+        for tensor, dst in ((synth.Q_ID, self.q), (synth.K_ID, self.k), (synth.V_ID, self.v)):
+            for h, x in zip(heads, synth.gen_heads(wl, tensor, heads, threads)):
+                dst[:, h, :].copy_(torch.from_numpy(x).to(self.dtype), non_blocking=False)
+        self.a2v.copy_(torch.from_numpy(synth.gen_a2v(wl)))
+        if self.train:
+            for h, x in zip(heads, synth.gen_heads(wl, synth.DO_ID, heads, threads)):
+                self.do_blk[:, h, :].copy_(torch.from_numpy(x).to(self.dtype))
+        torch.cuda.synchronize(self.device)
+
+    # ------------------------------------------------------------------- steps
+    def zone_shapes(self, stream=None):
+        wl = self.wl
+        feat = self.v.view(wl.N, wl.heads * wl.d)
+        self.ws_zone = P.prism_zone_shapes(feat, wl.heads * wl.d, self.a2v, wl.grid, wl.zone, wl.shapes,
+                                           self.zone_shape, self.perm, self.ws_zone, stream)
+
+    def pool_score(self, stream=None):
+        P.prism_pool_score(self.q, self.k, self.v, self.perm, self.wl.block, self.q_blk, self.k_blk, self.v_blk,
+                           self.qbar, self.kbar, self.scores, stream)
+
+    def select(self, stream=None):
+        P.prism_select(self.scores, self.sparsity, self.wl.cdf_tau, self.counts, self.idx, stream)
+
+    def _groups(self):
+        g = self.wl.head_group or self.wl.heads
+        return [(h0, min(h0 + g, self.wl.heads)) for h0 in range(0, self.wl.heads, g)]
+
+    def attention_fwd(self, stream=None):
+        B = self.wl.block
+        for h0, h1 in self._groups():
+            self.ws_fwd = P.prism_bsa_fwd(self.q_blk[:, h0:h1], self.k_blk[:, h0:h1], self.v_blk[:, h0:h1], B,
+                                          self.counts[h0:h1], self.idx[h0:h1], self.o_blk[:, h0:h1],
+                                          self.lse[h0:h1], self.ws_fwd, stream)
+
+    def attention_bwd(self, stream=None):
+        B = self.wl.block
+        for h0, h1 in self._groups():
+            self.ws_bwd = P.prism_bsa_bwd(self.q_blk[:, h0:h1], self.k_blk[:, h0:h1], self.v_blk[:, h0:h1],
+                                          self.o_blk[:, h0:h1], self.do_blk[:, h0:h1], self.lse[h0:h1], B,
+                                          self.counts[h0:h1], self.idx[h0:h1], self.dq[:, h0:h1],
+                                          self.dk[:, h0:h1], self.dv[:, h0:h1], self.ws_bwd, stream)
+
+    def forward(self, stream=None):
+        self.zone_shapes(stream)
+        self.pool_score(stream)
+        self.select(stream)
+        self.attention_fwd(stream)
+
+    def step(self, stream=None):
+        """One pass of the whole path: forward, plus backward when training."""
+        self.forward(stream)
+        if self.train:
+            self.attention_bwd(stream)
+
+    # ------------------------------------------------------------------- work
+    def executed_pairs(self) -> np.ndarray:
+        """Per (head, query block): sum over kept blocks of |b_i| * |b_j| (token pairs)."""
+        wl = self.wl
+        lens = torch.full((wl.nb,), wl.block, dtype=torch.int64, device=self.device)
+        lens[-1] = wl.N - wl.block * (wl.nb - 1)
+        nbr = torch.arange(wl.nb, device=self.device)
+        valid = nbr[None, None, :] < self.counts[:, :, None].long()
+        jl = lens[self.idx.long().clamp(0, wl.nb - 1)] * valid
+        return (jl.sum(-1) * lens[None, :]).cpu().numpy()
+
+    def flops(self):
+        """(executed fwd FLOPs, executed bwd FLOPs, dense-equivalent fwd, dense bwd)."""
+        wl = self.wl
+        pairs = float(self.executed_pairs().sum())
+        dense = float(wl.N) * wl.N * wl.heads
+        return 4.0 * pairs * wl.d, 10.0 * pairs * wl.d, 4.0 * dense * wl.d, 10.0 * dense * wl.d

@@ -1,0 +1,201 @@
+/*
+ * prism.h -- C ABI of libprism.so: Prism-style dynamic block-sparse self-attention
+ * over 3D (t, h, w) video-latent tokens, for NVIDIA B300 (sm_103a).
+ *
+ * Source of the method: "Prism: dynamic sparse attention for 2K joint video-audio
+ * generation training" (trawling.dev/post/2299), section "Region-adapted block
+ * construction".  Paragraph 1: tokens are grouped into spatio-temporal macro-zones;
+ * per zone, the channel-wise variance of the video features and the feature norm
+ * of the audio-to-video cross-attention set the zone's block shape, splitting more
+ * finely along axes of fast video change or strong audio-video coupling.
+ * Paragraph 2: a hybrid block selection makes each query's sparsity dynamic;
+ * Prism Block Sparse Attention (BSA) runs on the selected blocks; the settings use
+ * sparsity 0.75 / 0.80 / 0.85 / 0.93 and a CDF threshold of 0.20.
+ * The page gives no formulas; every reading taken where it is silent is stated at
+ * the call it concerns.
+ *
+ * Conventions shared by every call
+ *   - All array arguments are CUDA device pointers owned by the caller unless a
+ *     comment says "host".  The library never frees, keeps or allocates them, and
+ *     allocates no device memory of its own: scratch space comes from the caller's
+ *     workspace `ws` (query its size by passing ws = NULL; *ws_bytes receives it).
+ *   - Every call enqueues its kernels on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns without synchronising.  Buffers must stay valid
+ *     until the stream has executed the work.
+ *   - Token grid (T, H, W), N = T*H*W tokens.  "Raster order": token n = (t*H + h)*W + w.
+ *     "Block order": the order given by `perm` (see prism_zone_shapes); block b is
+ *     the B consecutive block-order tokens [b*B, min((b+1)*B, N)), nb = ceil(N/B);
+ *     only the last block can be short.
+ *   - Per-head tensors are [N][Hh][d] row-major with a token row stride `ld`
+ *     (elements, >= Hh*d, multiple of 8): element (n, h, c) is at n*ld + h*d + c.
+ *     A group of heads of a larger tensor is addressed by offsetting the pointer by
+ *     h0*d elements and keeping ld.  Pointers to bf16 data must be 16-byte aligned.
+ *   - Status: 0 = PRISM_OK; other values as below.  On an error nothing is enqueued
+ *     and prism_last_error() describes it.  Device-side conditions (a bounded wait
+ *     that gave up, an out-of-range block index that was skipped) are recorded in a
+ *     device status word read by prism_status_check().
+ */
+#ifndef PRISM_H
+#define PRISM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  PRISM_OK = 0,
+  PRISM_EINVAL = 1,        /* bad size, pointer, alignment or argument value        */
+  PRISM_EUNSUPPORTED = 2,  /* valid request outside what this build implements      */
+  PRISM_ECUDA = 3,         /* a CUDA runtime call or kernel launch failed           */
+  PRISM_ETIMEOUT = 4,      /* (status word) a bounded device wait gave up           */
+  PRISM_EINDEX = 5         /* (status word) an out-of-range block index was skipped */
+};
+
+enum { PRISM_F32 = 0, PRISM_BF16 = 1 };
+
+/* Bits of the device status word returned by prism_status_check(). */
+enum { PRISM_DEV_TIMEOUT = 1u, PRISM_DEV_BAD_INDEX = 2u, PRISM_DEV_TMEM = 4u };
+
+/*
+ * prism_zone_shapes -- step 1: per-macro-zone block shape and the block-order
+ * permutation (Prism page, "Region-adapted block construction", paragraph 1).
+ *
+ * Readings where the page is silent:
+ *   zones of extent (zt, zh, zw) tile the grid from the origin; the last zone on
+ *   an axis is clipped; zones are numbered in raster order of (zone_t, zone_h, zone_w).
+ *   v_a(z) = mean over channels and over the zone's lines along axis a of the
+ *            population variance of the feature along the line (0 for length 1);
+ *   u_a(z) = mean over the zone's lines along axis a of the population variance of
+ *            the A2V norm field; abar(z) = zone mean of the field;
+ *   w(z)   = abar(z) / max_z abar (0 if that max is 0);
+ *   S_a    = v_a / sum_b v_b + w * u_a / sum_b u_b  (0/0 := 0);
+ *   shape  = argmin over the shape set of sum_a S_a * log2(e_a), first index on ties
+ *            (costs compared in fp32).
+ *   Block order: zones in raster order; inside a zone, tiles of the chosen shape in
+ *   tile-raster order, clipped at the zone edge; inside a tile, tokens in raster order.
+ *
+ * feat       [N][feat_ld] raster order, `feat_dtype` PRISM_F32 or PRISM_BF16; the
+ *            first C channels of each row are the video feature (e.g. V, all heads).
+ * a2v        [N] fp32 raster order: A2V cross-attention feature-norm field.
+ * shapes     HOST [n_shapes][3] int32 (e_t, e_h, e_w), each >= 1; 1 <= n_shapes <= 8.
+ * zone_shape out [Z] int32, Z = ceil(T/zt)*ceil(H/zh)*ceil(W/zw): chosen shape index.
+ * perm       out [N] int32: perm[r] = raster index of the token at block-order position r.
+ * ws         workspace of *ws_bytes bytes (NULL = size query).  Alignment 256 bytes.
+ */
+int prism_zone_shapes(const void* feat, int32_t feat_dtype, int64_t feat_ld, int32_t C,
+                      const float* a2v, int32_t T, int32_t H, int32_t W,
+                      int32_t zt, int32_t zh, int32_t zw,
+                      const int32_t* shapes, int32_t n_shapes,
+                      int32_t* zone_shape, int32_t* perm,
+                      void* ws, size_t* ws_bytes, void* stream);
+
+/*
+ * prism_pool_score -- step 2: block-mean pooling of Q and K and block scores.
+ * The page names "block-level features"; the reading is the block mean (true
+ * length for the short last block) and the score qbar . kbar / sqrt(d).
+ *
+ * q, k, v    [N][Hh][d] with row stride ld, in raster order if perm != NULL (then
+ *            the block-order copies below are written), else already in block order.
+ * dtype      PRISM_F32 or PRISM_BF16 for q, k, v and the copies.
+ * perm       [N] int32 from prism_zone_shapes, or NULL.
+ * q_blk, k_blk, v_blk  out [N][Hh][d], row stride ld_blk: block-order copies
+ *            (row r = input row perm[r]); each may be NULL to skip it; must all be
+ *            NULL when perm is NULL.  v may be NULL when v_blk is NULL.
+ * qbar, kbar out [Hh][nb][d] fp32 block means (either may be NULL).
+ * scores     out [Hh][nb][nb] fp32: scores[h][i][j] = qbar[h][i] . kbar[h][j] / sqrt(d);
+ *            may be NULL; when given, qbar and kbar must be given too.
+ * Limits: d <= 256, B >= 1.
+ */
+int prism_pool_score(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld,
+                     const int32_t* perm, int32_t N, int32_t Hh, int32_t d, int32_t B,
+                     void* q_blk, void* k_blk, void* v_blk, int64_t ld_blk,
+                     float* qbar, float* kbar, float* scores, void* stream);
+
+/*
+ * prism_select -- step 3: hybrid block selection (Prism page, "Region-adapted
+ * block construction", paragraph 2).  Reading: per (head h, query block i), with
+ * blocks ordered by score descending (equal scores: smaller index first),
+ *   k = min(nb, max(1, ceil((1 - sparsity) * nb - 1e-9)))   (top-(1-s) fraction),
+ *   m = the shortest prefix whose softmax mass (softmax over the row) reaches cdf_tau,
+ * and the kept set is the union, i.e. the first max(k, m) blocks of that order.
+ *
+ * scores  [Hh][nb][nb] fp32.   sparsity in [0, 1); cdf_tau in [0, 1].
+ * counts  out [Hh][nb] int32: number of kept blocks.
+ * idx     out [Hh][nb][nb] int32: idx[h][i][0:counts[h][i]] = kept blocks, ascending;
+ *         the rest of each row is left untouched.
+ * Limits: 1 <= nb <= 4096.
+ */
+int prism_select(const float* scores, int32_t Hh, int32_t nb, double sparsity, double cdf_tau,
+                 int32_t* counts, int32_t* idx, void* stream);
+
+/*
+ * prism_bsa_fwd -- step 4: block-sparse attention forward (Prism BSA, same page,
+ * paragraph 2).  For every head h and query block i, each query token r attends to
+ * all tokens c of the blocks idx[h][i][0:counts[h][i]]:
+ *   O[r] = sum_c softmax_c(Q[r].K[c] / sqrt(d)) V[c],  lse[h][r] = log sum_c exp(Q[r].K[c] / sqrt(d)).
+ * No causal mask.  A query block with an empty list gets O = 0 and lse = -inf.
+ *
+ * q_blk, k_blk, v_blk  [N][Hh][d] block order, row stride ld, dtype PRISM_BF16
+ *         (tensor-core path for d = 128, B = 128; CUDA-core path otherwise) or
+ *         PRISM_F32 (CUDA-core path).
+ * counts  [Hh][nb] int32;  idx [Hh][nb][nb] int32 (row stride nb), nb = ceil(N/B).
+ *         Entries outside [0, nb) are skipped and flagged PRISM_DEV_BAD_INDEX.
+ * o_blk   out [N][Hh][d], row stride ld, same dtype as the inputs.
+ * lse     out [Hh][N] fp32 (natural log).
+ * ws      workspace (NULL = size query).
+ * Limits: d in {64, 128}; B in {64, 128}; the tensor-core path needs d = B = 128.
+ */
+int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32_t dtype,
+                  int64_t ld, int32_t N, int32_t Hh, int32_t d, int32_t B,
+                  const int32_t* counts, const int32_t* idx, int32_t nb,
+                  void* o_blk, float* lse, void* ws, size_t* ws_bytes, void* stream);
+
+/*
+ * prism_bsa_bwd -- step 5: gradients of block-sparse attention for training (the
+ * page trains with Prism BSA switched on).  With the same kept lists as the
+ * forward, treated as constants (no gradient through selection):
+ *   P = exp(Q K^T / sqrt(d) - lse), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
+ *   dS = P * (dP - D), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d).
+ *
+ * q_blk .. do_blk  [N][Hh][d] block order, row stride ld, dtype as in the forward.
+ * lse     [Hh][N] fp32 from prism_bsa_fwd.
+ * dq, dk, dv  out [N][Hh][d], row stride ld, same dtype.
+ * ws      workspace (NULL = size query): transposed lists and row statistics.
+ * Limits as prism_bsa_fwd.
+ */
+int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk,
+                  const void* o_blk, const void* do_blk, const float* lse, int32_t dtype,
+                  int64_t ld, int32_t N, int32_t Hh, int32_t d, int32_t B,
+                  const int32_t* counts, const int32_t* idx, int32_t nb,
+                  void* dq, void* dk, void* dv, void* ws, size_t* ws_bytes, void* stream);
+
+/*
+ * prism_status_check -- synchronise `stream`, return PRISM_OK if the device status
+ * word is clear, else PRISM_ETIMEOUT or PRISM_EINDEX (the first set condition), and
+ * clear the word.  *word (may be NULL) receives the raw PRISM_DEV_* bits.
+ */
+int prism_status_check(void* stream, uint32_t* word);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+const char* prism_last_error(void);
+
+/* Build description: version, target architecture, compile-time limits. */
+const char* prism_build_info(void);
+
+/*
+ * Diagnostics: prism_selftest_umma runs one 128 x 128 x 128 tile through the same
+ * tensor-core operand layouts the attention kernels use: out_s = A B^T (A, B from
+ * shared memory, K-major, 128-byte swizzle) and out_o = bf16(out_s) B (A operand
+ * from tensor memory, B read MN-major).  a, b: [128][128] bf16 row-major device
+ * arrays (16-byte aligned); out_s, out_o: [128][128] fp32.  `variant` 0 is the
+ * layout the kernels use; 1 swaps the two byte offsets of the MN-major descriptor.
+ */
+int prism_selftest_umma(const void* a, const void* b, float* out_s, float* out_o, int32_t variant, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PRISM_H */
