@@ -2,6 +2,7 @@
 // sizing, dispatch to the kernel launchers, and the device status word.
 //
 // Nothing here allocates device memory: scratch space is the caller's workspace.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -22,6 +23,13 @@ namespace {
 __device__ uint32_t g_status_word;
 
 thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+// Count the kernels a successful call enqueued.
+int launched(int n) {
+  g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed);
+  return PRISM_OK;
+}
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -141,7 +149,7 @@ int prism_zone_shapes(const void* feat, int32_t feat_dtype, int64_t feat_ld, int
   if (!feat || !a2v || !zone_shape || !perm) return fail(PRISM_EINVAL, "NULL pointer");
   cudaError_t e = prism::zone_launch(feat, feat_dtype, feat_ld, C, a2v, g, ss, zone_shape, perm, ws,
                                      static_cast<cudaStream_t>(stream), status_ptr());
-  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_zone_shapes");
+  return e == cudaSuccess ? (launched(4), ok()) : cuda_fail(e, "prism_zone_shapes");
 }
 
 int prism_pool_score(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld, const int32_t* perm,
@@ -164,7 +172,9 @@ int prism_pool_score(const void* q, const void* k, const void* v, int32_t dtype,
     e = prism::pool_launch(q, k, v, dtype, ld, perm, N, Hh, d, B, q_blk, k_blk, v_blk, copies ? ld_blk : ld, qbar,
                            kbar, st, status_ptr());
   if (e == cudaSuccess && scores) e = prism::scores_launch(qbar, kbar, Hh, nb, d, scores, st);
-  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_pool_score");
+  if (e != cudaSuccess) return cuda_fail(e, "prism_pool_score");
+  launched((qbar || kbar || copies ? 1 : 0) + (scores ? 1 : 0));
+  return ok();
 }
 
 int prism_select(const float* scores, int32_t Hh, int32_t nb, double sparsity, double cdf_tau, int32_t* counts,
@@ -178,7 +188,7 @@ int prism_select(const float* scores, int32_t Hh, int32_t nb, double sparsity, d
   const int k_top = (int)std::min<double>(nb, std::max<double>(1.0, kk));
   cudaError_t e = prism::select_launch(scores, Hh, nb, k_top, (float)cdf_tau, counts, idx,
                                        static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_select");
+  return e == cudaSuccess ? (launched(1), ok()) : cuda_fail(e, "prism_select");
 }
 
 int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32_t dtype, int64_t ld, int32_t N,
@@ -195,7 +205,7 @@ int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32
   else
     e = prism::bsa_fwd_simt_launch(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb, o_blk, lse, st,
                                    status_ptr());
-  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_bsa_fwd");
+  return e == cudaSuccess ? (launched(1), ok()) : cuda_fail(e, "prism_bsa_fwd");
 }
 
 int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk, const void* o_blk, const void* do_blk,
@@ -216,7 +226,7 @@ int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk, const
   if (e == cudaSuccess)
     e = prism::bsa_bwd_simt_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, dtype, ld, N, Hh, d, B, counts, idx,
                                    nb, dq, dk, dv, tcounts, tidx, Drow, st, status_ptr());
-  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_bsa_bwd");
+  return e == cudaSuccess ? (launched(5), ok()) : cuda_fail(e, "prism_bsa_bwd");
 }
 
 int prism_status_check(void* stream, uint32_t* word) {
@@ -237,6 +247,8 @@ int prism_status_check(void* stream, uint32_t* word) {
 }
 
 const char* prism_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t prism_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* prism_build_info(void) {
   return "libprism 0.1 | sm_103a | bsa_fwd: tcgen05+TMA for bf16 d=128 B=128, CUDA cores otherwise | "

@@ -53,14 +53,15 @@ class PrismLayer:
     def load_inputs(self, threads=8):
         """Generate the seeded inputs on the host and copy them into the device buffers."""
         wl = self.wl
-        heads = list(range(wl.heads))
-        for tensor, dst in ((synth.Q_ID, self.q), (synth.K_ID, self.k), (synth.V_ID, self.v)):
-            for h, x in zip(heads, synth.gen_heads(wl, tensor, heads, threads)):
-                dst[:, h, :].copy_(torch.from_numpy(x).to(self.dtype), non_blocking=False)
-        self.a2v.copy_(torch.from_numpy(synth.gen_a2v(wl)))
+        todo = [(synth.Q_ID, self.q), (synth.K_ID, self.k), (synth.V_ID, self.v)]
         if self.train:
-            for h, x in zip(heads, synth.gen_heads(wl, synth.DO_ID, heads, threads)):
-                self.do_blk[:, h, :].copy_(torch.from_numpy(x).to(self.dtype))
+            todo.append((synth.DO_ID, self.do_blk))
+        for tensor, dst in todo:
+            for h0 in range(0, wl.heads, 8):   # groups of heads bound the host memory
+                heads = list(range(h0, min(h0 + 8, wl.heads)))
+                for h, x in zip(heads, synth.gen_heads(wl, tensor, heads, threads)):
+                    dst[:, h, :].copy_(torch.from_numpy(x).to(self.dtype))
+        self.a2v.copy_(torch.from_numpy(synth.gen_a2v(wl)))
         torch.cuda.synchronize(self.device)
 
     # ------------------------------------------------------------------- steps

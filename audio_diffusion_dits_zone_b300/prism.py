@@ -31,6 +31,7 @@ _SIGS = {
                       _P],
     "prism_status_check": [_P, ctypes.POINTER(ctypes.c_uint32)],
     "prism_last_error": [],
+    "prism_launch_count": [],
     "prism_build_info": [],
     "prism_selftest_umma": [_P, _P, _P, _P, _I32, _P],
 }
@@ -55,6 +56,8 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.argtypes = args
             f.restype = ctypes.c_char_p if name in ("prism_last_error", "prism_build_info") else ctypes.c_int
+            if name == "prism_launch_count":
+                f.restype = ctypes.c_uint64
         _lib = L
     return _lib
 
@@ -92,6 +95,11 @@ def _ld(t):
     """Token row stride (elements) of a [N, Hh, d] view with contiguous heads."""
     assert t.dim() == 3 and t.stride(2) == 1 and t.stride(1) == t.shape[2], "need a [N, Hh, d] view, d contiguous"
     return t.stride(0)
+
+
+def launch_count() -> int:
+    """Kernels the library has enqueued so far."""
+    return int(lib().prism_launch_count())
 
 
 def build_info() -> str:

@@ -1,0 +1,385 @@
+"""Benchmark of one Prism block-sparse attention layer, forward + backward, on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload train720p] [--sparsity 0.8]
+
+A step is one pass of the whole path over one batch of synthetic input: zone
+shapes -> pool + score -> hybrid select -> block-sparse attention forward ->
+backward, for all heads of one layer.  Default workload: the 720p training step
+(T=21, H=45, W=80 = 75,600 tokens, 40 heads, d = 128, bf16, sparsity 0.80, CDF 0.20).
+Inputs are generated from seeds, copied to HBM before timing, and are larger than
+L2 (Q, K, V, dO: 774 MB each), so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  value = executed-block attention TFLOP/s of the
+whole step (forward 4*|b_i|*|b_j|*d + backward 10*|b_i|*|b_j|*d per kept block
+pair, divided by the step time); for N GPUs (torchrun) every rank runs its own
+replica of the workload and value = total work / max-over-ranks time.
+--impl reference times the CPU oracle on the host cores on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-sparse attn fwd+bwd ms/layer & effective TFLOPS (% bf16 peak), 720p–2K"
+UNIT = "TFLOP/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16": 1800.0, "bf16_sustained": 1400.0, "source": "fallback"}
+
+
+def workload_config(wl, sparsity):
+    return {"workload": f"{wl.name}: Prism layer fwd+bwd, T={wl.grid[0]},H={wl.grid[1]},W={wl.grid[2]} "
+                        f"({wl.N} tokens), {wl.heads} heads, d={wl.d}, {wl.dtype}, B={wl.block}, "
+                        f"zones {wl.zone[0]}x{wl.zone[1]}x{wl.zone[2]}, sparsity {sparsity}, CDF {wl.cdf_tau}",
+            "global_batch": 1, "seq_len": wl.N, "heads": wl.heads, "head_dim": wl.d, "sparsity": sparsity,
+            "cdf_tau": wl.cdf_tau, "parallelism": "replicas (one layer per GPU)",
+            "l2": "inputs larger than L2 (Q, K, V, dO 774 MB each); no flush"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        load = [s for s in sm if s > 0.5 * mx] or sm
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+# ----------------------------------------------------------------- ours
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from audio_diffusion_dits_zone_b300 import prism as P
+    from audio_diffusion_dits_zone_b300 import synth
+    from audio_diffusion_dits_zone_b300.pipeline import PrismLayer
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = synth.WORKLOADS[args.workload]
+    sp = wl.sparsity if args.sparsity is None else args.sparsity
+    layer = PrismLayer(wl, dev, sparsity=sp, train=True)
+    layer.load_inputs()
+    layer.step()
+    if P.status_check() != 0:
+        raise RuntimeError("device status word set after the first step")
+    fwd_fl, bwd_fl, dense_f, dense_b = layer.flops()
+    work = fwd_fl + bwd_fl
+    names = ["zone_shapes", "pool_score", "select", "bsa_fwd", "bsa_bwd"]
+    calls = [layer.zone_shapes, layer.pool_score, layer.select, layer.attention_fwd, layer.attention_bwd]
+    for _ in range(args.warmup):
+        layer.step()
+    torch.cuda.synchronize()
+    # ---------------- timed region: K steps, events around every call on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    launches0 = P.launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for s in range(args.steps):
+            ev[s][0].record()
+            for c, fn in enumerate(calls):
+                fn()
+                ev[s][c + 1].record()
+        t1.record()
+        torch.cuda.synchronize()
+    launches = P.launch_count() - launches0
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        torch.distributed.barrier()
+    if P.status_check() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    per_call = {n: statistics.mean(ev[s][c].elapsed_time(ev[s][c + 1]) for s in range(args.steps))
+                for c, n in enumerate(names)}
+    ms = elapsed_ms / args.steps
+    pk = peaks()
+    value = world * work / (ms * 1e-3) / 1e12
+
+    # dominant kernel: the call that takes the longest (both attention calls are tensor-bound)
+    dom = max(("bsa_fwd", "bsa_bwd"), key=lambda n: per_call[n])
+    dom_flops = fwd_fl if dom == "bsa_fwd" else bwd_fl
+    achieved = dom_flops / (per_call[dom] * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get(f"{wl.name}:{dom}")
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": pk["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sustained"], 4), "traffic": traffic,
+                "peak_note": f"bf16 dense, sustained ({pk['source']}); burst {pk['bf16']}",
+                "frac_of_burst": round(achieved / pk["bf16"], 4)}
+    hbm = {}
+    algo_bytes = {
+        "zone_shapes": wl.N * wl.heads * wl.d * 2 + wl.N * 4 + wl.N * 4,
+        "pool_score": 3 * wl.N * wl.heads * wl.d * 2 * 2 + 2 * wl.heads * wl.nb * wl.d * 4 + wl.heads * wl.nb ** 2 * 4,
+        "select": wl.heads * wl.nb ** 2 * 4 + wl.heads * wl.nb * 4 + 4 * int(layer.counts.sum().item()),
+    }
+    for n, b in algo_bytes.items():
+        gbs = b / (per_call[n] * 1e-3) / 1e9
+        hbm[n] = {"ms": round(per_call[n], 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+
+    # ---------------- end to end through the public API, host buffers
+    e2e = run_e2e(layer, args, world)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Wan-VAE-shaped latents, no weights)",
+        "config": workload_config(wl, sp),
+        "ms_per_layer": round(ms, 3),
+        "tflops_executed": round(work / (ms * 1e-3) / 1e12, 3),
+        "tflops_dense_equivalent": round((dense_f + dense_b) / (ms * 1e-3) / 1e12, 3),
+        "pct_bf16_peak_executed": round(100 * work / (ms * 1e-3) / 1e12 / pk["bf16_sustained"], 2),
+        "per_call_ms": {n: round(v, 4) for n, v in per_call.items()},
+        "attention_tflops": {"bsa_fwd": round(fwd_fl / (per_call["bsa_fwd"] * 1e-3) / 1e12, 2),
+                             "bsa_bwd": round(bwd_fl / (per_call["bsa_bwd"] * 1e-3) / 1e12, 2)},
+        "hbm_bound_calls": hbm,
+        "kept_fraction": round(float(layer.counts.double().mean().item()) / wl.nb, 4),
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, sp, budget_s=args.cpu_seconds)
+    return line
+
+
+def run_e2e(layer, args, world):
+    """Same step through the public API with host buffers: H2D of the inputs from
+    pinned memory, the step, D2H of the results (O, dQ, dK, dV) each step."""
+    import torch
+
+    ins = [layer.q, layer.k, layer.v, layer.a2v, layer.do_blk]
+    outs = [layer.o_blk, layer.dq, layer.dk, layer.dv]
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
+    for h, t in zip(h_in, ins):
+        h.copy_(t)
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    steps = max(2, min(args.steps, 5))
+
+    def one():
+        for h, t in zip(h_in, ins):
+            t.copy_(h, non_blocking=True)
+        layer.step()
+        for h, t in zip(h_out, outs):
+            h.copy_(t, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    if world > 1:
+        t = torch.tensor([dt], device=layer.device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    fwd_fl, bwd_fl, _, _ = layer.flops()
+    return {"value": round(world * (fwd_fl + bwd_fl) / dt / 1e12, 3), "unit": UNIT, "ms_per_step": round(dt * 1e3, 3),
+            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in ins)),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs)), "steps": steps}
+
+
+# ------------------------------------------------------------ the oracle
+def oracle_sample_step(wl, sp, ctx, qblocks):
+    """One bounded sample of the step on the CPU oracle: block means and scores of one
+    head, selection of the sampled query blocks, and their attention forward and
+    backward (dQ of the sample, dK/dV contributions of the sample)."""
+    import numpy as np
+
+    from oracle import prism_oracle as po
+
+    Qb, Kb, Vb, dOb = ctx
+    qbar = po.block_mean(Qb, wl.block)
+    kbar = po.block_mean(Kb, wl.block)
+    S = po.block_scores(qbar[:, qblocks], kbar)
+    counts = np.zeros((1, wl.nb), np.int32)
+    idx = np.zeros((1, wl.nb, wl.nb), np.int32)
+    pairs = 0
+    for r, i in enumerate(qblocks):
+        kept, _, _ = po.select_row(S[0, r], sp, wl.cdf_tau)
+        counts[0, i] = kept.size
+        idx[0, i, : kept.size] = kept
+        lens = np.minimum(wl.block, wl.N - kept * wl.block)
+        pairs += int(lens.sum()) * min(wl.block, wl.N - i * wl.block)
+    po.bsa_forward(Qb, Kb, Vb, counts, idx, wl.block, qblocks=qblocks)
+    po.bsa_backward_sampled(Qb, Kb, Vb, dOb, counts, idx, wl.block, 0, qblocks, [])
+    return 14.0 * pairs * wl.d
+
+
+def oracle_context(wl, head):
+    """Head `head` of Q, K, V, dO in block order ([N, 1, d] fp64).  The block order comes
+    from the oracle's zone statistics over this head's channels of V (a sample of the
+    zone step, computed once, outside any timing)."""
+    import numpy as np
+
+    from audio_diffusion_dits_zone_b300 import synth
+    from oracle import prism_oracle as po
+
+    hs = [head]
+    Q, K, V = (np.stack(synth.gen_heads(wl, t, hs), axis=1).astype(np.float64)
+               for t in (synth.Q_ID, synth.K_ID, synth.V_ID))
+    dO = np.stack(synth.gen_heads(wl, synth.DO_ID, hs), axis=1).astype(np.float64)
+    _, perm, _ = po.zone_shapes([V[:, 0]], synth.gen_a2v(wl), wl.grid, wl.zone, wl.shapes)
+    return Q[perm], K[perm], V[perm], dO
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, sp, budget_s=20.0, head=0):
+    """The oracle as it stands, timed on the host cores on a bounded sample."""
+    ctx = oracle_context(wl, head)
+    blocks = list(range(0, wl.nb, max(1, wl.nb // 64)))
+    done, work, t0 = 0, 0.0, time.perf_counter()
+    while done < len(blocks) and time.perf_counter() - t0 < budget_s:
+        work += oracle_sample_step(wl, sp, ctx, blocks[done:done + 2])
+        done += 2
+    dt = time.perf_counter() - t0
+    return {"value": round(work / dt / 1e12, 6), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"head {head}: block means/scores, selection and attention fwd+bwd of {done} query blocks "
+                      f"(of {wl.nb}) spread over the sequence; {dt:.1f} s of CPU time; zone statistics "
+                      f"over this head's channels done once outside the timing"}
+
+
+def run_reference(args):
+    from audio_diffusion_dits_zone_b300 import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    sp = wl.sparsity if args.sparsity is None else args.sparsity
+    ctx = oracle_context(wl, 0)
+    blocks = list(range(0, wl.nb, max(1, wl.nb // 64)))
+    per = 2
+    for w in range(args.warmup):
+        oracle_sample_step(wl, sp, ctx, blocks[(w * per) % len(blocks):][:per])
+    work, t0 = 0.0, time.perf_counter()
+    for s in range(args.steps):
+        b = blocks[(s * per) % len(blocks):][:per]
+        work += oracle_sample_step(wl, sp, ctx, b)
+    dt = time.perf_counter() - t0
+    v = work / dt / 1e12
+    sample = (f"each step: head 0, block means/scores, selection and attention fwd+bwd of {per} query blocks "
+              f"(of {wl.nb}); fp64 numpy")
+    return {"metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, sp), "impl": "reference",
+            "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="train720p")
+    ap.add_argument("--sparsity", type=float, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

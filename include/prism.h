@@ -182,6 +182,10 @@ int prism_status_check(void* stream, uint32_t* word);
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 const char* prism_last_error(void);
 
+/* Number of kernels the library has enqueued since it was loaded (all devices and
+ * threads): a counter for measuring how many launches a step makes. */
+uint64_t prism_launch_count(void);
+
 /* Build description: version, target architecture, compile-time limits. */
 const char* prism_build_info(void);
 
