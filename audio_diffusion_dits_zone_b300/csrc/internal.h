@@ -7,6 +7,9 @@
 
 namespace prism {
 
+// Record `msg` as the calling thread's last error (prism_last_error) and return `code`.
+int report_error(int code, const char* msg);
+
 struct ZoneGeom {
   int T, H, W;      // token grid
   int zt, zh, zw;   // zone extents

@@ -117,6 +117,10 @@ bool use_tc(int32_t dtype, int32_t d, int32_t B, int64_t ld, std::initializer_li
 
 }  // namespace
 
+namespace prism {
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace prism
+
 extern "C" {
 
 int prism_zone_shapes(const void* feat, int32_t feat_dtype, int64_t feat_ld, int32_t C, const float* a2v, int32_t T,

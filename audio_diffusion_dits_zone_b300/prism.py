@@ -24,6 +24,8 @@ _I64 = ctypes.c_int64
 _SZ = ctypes.POINTER(ctypes.c_size_t)
 _SIGS = {
     "prism_zone_shapes": [_P, _I32, _I64, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P, _P, _P, _SZ, _P],
+    "prism_zone_shapes_noalloc": [_P, _I32, _I64, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P, _P,
+                                  _P],
     "prism_pool_score": [_P, _P, _P, _I32, _I64, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _P, _P, _P, _P],
     "prism_select": [_P, _I32, _I32, ctypes.c_double, ctypes.c_double, _P, _P, _P],
     "prism_bsa_fwd": [_P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P],
@@ -138,6 +140,18 @@ def prism_zone_shapes(feat, C, a2v, grid, zone, shapes, zone_shape, perm, ws=Non
     ws, nbytes = _ws(call, ws, feat.device)
     _check(call(_ptr(ws), ctypes.byref(nbytes)))
     return ws
+
+
+def prism_zone_shapes_noalloc(feat, C, a2v, grid, zone, shapes, zone_shape, perm, stream=None):
+    """Zone shapes and permutation with no workspace: the library's built-in scratch is used.
+
+    For callers that cannot provide device memory; calls on one device must not
+    overlap on the GPU (they share the scratch)."""
+    assert feat.dim() == 2 and feat.stride(1) == 1
+    T, H, W = grid
+    sh = (ctypes.c_int32 * (3 * len(shapes)))(*[int(e) for s in shapes for e in s])
+    _check(lib().prism_zone_shapes_noalloc(_ptr(feat), _dtype(feat), feat.stride(0), C, _ptr(a2v), T, H, W, *zone,
+                                           sh, len(shapes), _ptr(zone_shape), _ptr(perm), _stream(stream)))
 
 
 # ------------------------------------------------------------------- step 2

@@ -93,6 +93,25 @@ int prism_zone_shapes(const void* feat, int32_t feat_dtype, int64_t feat_ld, int
                       void* ws, size_t* ws_bytes, void* stream);
 
 /*
+ * prism_zone_shapes_noalloc -- the same computation and outputs as
+ * prism_zone_shapes, for callers that cannot give the library device memory (their
+ * device memory belongs to another allocator, or they run in a hook that must not
+ * allocate).  The page has no counterpart of this call; it only changes where the
+ * scratch lives.  There is no workspace argument: the scratch is a fixed 1 MiB
+ * device array inside the library (held by every GPU that loads it until exit),
+ * enough for e.g. 700 zones x 5,120 feature channels.  Grids that need more return
+ * PRISM_EUNSUPPORTED with a message; use prism_zone_shapes with a workspace then.
+ * The first call on a device looks up the array's device address (make that first
+ * call before any stream capture).  All calls on a device share the array: calls
+ * that overlap on the GPU race and must be ordered by the caller.  Allocates nothing.
+ */
+int prism_zone_shapes_noalloc(const void* feat, int32_t feat_dtype, int64_t feat_ld, int32_t C,
+                              const float* a2v, int32_t T, int32_t H, int32_t W,
+                              int32_t zt, int32_t zh, int32_t zw,
+                              const int32_t* shapes, int32_t n_shapes,
+                              int32_t* zone_shape, int32_t* perm, void* stream);
+
+/*
  * prism_pool_score -- step 2: block-mean pooling of Q and K and block scores.
  * The page names "block-level features"; the reading is the block mean (true
  * length for the short last block) and the score qbar . kbar / sqrt(d).
