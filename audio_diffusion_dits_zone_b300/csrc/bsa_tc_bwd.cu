@@ -1,0 +1,524 @@
+// Step 5 of the path on the tensor cores: gradients of Prism Block Sparse Attention
+// for training, bf16, d = 128, 128-token blocks (sm_103a: TMA + tcgen05 + TMEM).
+//
+// "Prism: dynamic sparse attention for 2K joint video-audio generation training":
+// training runs with Prism BSA on (section "Region-adapted block construction",
+// paragraph 2; "Data preparation and training procedure").  With the kept lists
+// held constant:  P = exp(S - lse), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
+// dS = P * (dP - D), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d).
+//
+// Three kernels, no atomics (deterministic):
+//   bwd_prep  L2[h][r] = lse * log2(e) (+inf past the last token, so padded query
+//             rows get P = 0) and D[h][r], padded to whole blocks so the attention
+//             kernels can bulk-copy 128 of them at a time;
+//   dq        one CTA per (head, query block) walking its kept list:
+//               S_b = Q K_j^T (TMEM, double-buffered), dP = dO V_j^T (TMEM),
+//               dS = P (dP - D) in bf16 into the S buffer, dQ += dS K_j (A from TMEM);
+//   dkdv      one CTA per (head, key block) walking the query blocks that kept it:
+//               S^T = K_j Q_i^T, dP^T = V_j dO_i^T (TMEM),
+//               P^T, dS^T in bf16 into those buffers, dV += P^T dO_i, dK += dS^T Q_i.
+// The softmax-gradient warps work in two halves of 64 columns and release each half
+// as soon as it is written, so the MMAs of the first half overlap the arithmetic of
+// the second.  Warp roles as in the forward kernel: one TMA producer warp, one MMA
+// warp (TMEM owner), four warps that own one TMEM lane (row) each.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace prism {
+namespace {
+
+constexpr int kB = 128;
+constexpr int kD = 128;
+constexpr uint32_t kHalf = 16384;
+constexpr uint32_t kTile = 2 * kHalf;
+constexpr int kThreads = 192;  // warps: 0 producer, 1 MMA, 2-5 rows
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSl2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
+constexpr float kScale = 0.08838834764831845f;                      // 1 / sqrt(128)
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) {  // K-major operand, K step kk (16 elems)
+  return smem_desc(tile + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+}
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) {  // MN-major operand, K step kk (16 rows)
+  return smem_desc(tile + kk * 2048, kHalf, 1024, kSwizzle128B);
+}
+
+// ------------------------------------------------------------------- prep
+__global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
+                                const float* __restrict__ lse, int64_t ld, int N, int Hh, int npad,
+                                float* __restrict__ L2, float* __restrict__ Dp) {
+  // one warp per (head, padded row)
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= (int64_t)Hh * npad) return;
+  const int h = (int)(wid / npad), r = (int)(wid - (int64_t)h * npad);
+  float s = 0.f;
+  if (r < N) {
+    const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(o + (int64_t)r * ld + (int64_t)h * kD);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(dO + (int64_t)r * ld + (int64_t)h * kD);
+#pragma unroll
+    for (int c = lane; c < kD / 2; c += 32) {
+      const float2 x = __bfloat1622float2(a[c]), y = __bfloat1622float2(b[c]);
+      s = fmaf(x.x, y.x, fmaf(x.y, y.y, s));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) {
+    const size_t at = (size_t)h * npad + r;
+    Dp[at] = r < N ? s : 0.f;
+    L2[at] = r < N ? lse[(size_t)h * N + r] * kLog2e : INFINITY;
+  }
+}
+
+// --------------------------------------------------------------------- dQ
+struct DqSmem {
+  uint8_t q[kTile];
+  uint8_t dO[kTile];
+  uint8_t k[2][kTile];
+  uint8_t v[2][kTile];
+  uint64_t q_full;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full[2], dp_full;
+  uint64_t ds_a[2], ds_b[2];
+  uint64_t acc_done, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024;
+static_assert(kDqSmemBytes <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bsa_dq_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                     const float* __restrict__ L2, const float* __restrict__ Dp, int npad,
+                     __nv_bfloat16* __restrict__ dq, int64_t ld, int N, const int32_t* __restrict__ counts,
+                     const int32_t* __restrict__ idx, int nb, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x;
+  const int h = item / nb, i = item - h * nb;
+  int cnt = counts[item];
+  if (cnt < 0 || cnt > nb) cnt = cnt < 0 ? 0 : nb;
+  const int32_t* lst = idx + (size_t)item * nb;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.q_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&sm.kv_full[s]), 1);
+      mbar_init(smem_u32(&sm.kv_empty[s]), 1);
+      mbar_init(smem_u32(&sm.s_full[s]), 1);
+      mbar_init(smem_u32(&sm.ds_a[s]), 4);
+      mbar_init(smem_u32(&sm.ds_b[s]), 4);
+    }
+    mbar_init(smem_u32(&sm.dp_full), 1);
+    mbar_init(smem_u32(&sm.acc_done), 1);
+    mbar_init(smem_u32(&sm.mma_done), 1);
+    sm.abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;  // S0 [0,128) S1 [128,256) dP [256,384) dQ [384,512)
+  volatile int* abort = &sm.abort;
+
+  if (warp == 0) {
+    if (lane == 0 && cnt > 0) {
+      const uint32_t qb = smem_u32(&sm.q_full);
+      mbar_arrive_expect_tx(qb, 2 * kTile);
+      tma_load_2d(smem_u32(sm.q), &tmq, h * kD, i * kB, qb);
+      tma_load_2d(smem_u32(sm.q) + kHalf, &tmq, h * kD + 64, i * kB, qb);
+      tma_load_2d(smem_u32(sm.dO), &tmdo, h * kD, i * kB, qb);
+      tma_load_2d(smem_u32(sm.dO) + kHalf, &tmdo, h * kD + 64, i * kB, qb);
+      int armed[2] = {0, 0};
+      for (int it = 0; it < cnt; ++it) {
+        const int st = it & 1;
+        if (it >= 2 && !mbar_wait(smem_u32(&sm.kv_empty[st]), ((it >> 1) - 1) & 1, abort, status)) break;
+        int j = lst[it];
+        if (j < 0 || j >= nb) j = 0;
+        const uint32_t bar = smem_u32(&sm.kv_full[st]);
+        mbar_arrive_expect_tx(bar, 2 * kTile);
+        tma_load_2d(smem_u32(sm.k[st]), &tmk, h * kD, j * kB, bar);
+        tma_load_2d(smem_u32(sm.k[st]) + kHalf, &tmk, h * kD + 64, j * kB, bar);
+        tma_load_2d(smem_u32(sm.v[st]), &tmv, h * kD, j * kB, bar);
+        tma_load_2d(smem_u32(sm.v[st]) + kHalf, &tmv, h * kD + 64, j * kB, bar);
+        ++armed[st];
+      }
+      if (*abort) {
+        drain_wait(qb, 0);
+        for (int s = 0; s < 2; ++s)
+          if (armed[s]) drain_wait(smem_u32(&sm.kv_full[s]), (armed[s] - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && cnt > 0) {
+      constexpr uint32_t id_ss = idesc_bf16_f32(kB, kB, false, false);
+      constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
+      const uint32_t qa = smem_u32(sm.q), da = smem_u32(sm.dO);
+      bool ok = mbar_wait(smem_u32(&sm.q_full), 0, abort, status) &&
+                mbar_wait(smem_u32(&sm.kv_full[0]), 0, abort, status);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t ka = smem_u32(sm.k[0]), va = smem_u32(sm.v[0]);
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, kdesc(qa, kk), kdesc(ka, kk), id_ss, kk > 0);
+        tc_commit(smem_u32(&sm.s_full[0]));
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + 256, kdesc(da, kk), kdesc(va, kk), id_ss, kk > 0);
+        tc_commit(smem_u32(&sm.dp_full));
+      }
+      for (int it = 0; ok && it < cnt; ++it) {
+        const int b = it & 1, st = it & 1;
+        if (it + 1 < cnt) {
+          const int nst = (it + 1) & 1;
+          if (!(ok = mbar_wait(smem_u32(&sm.kv_full[nst]), ((it + 1) >> 1) & 1, abort, status))) break;
+          tc_fence_after();
+          const uint32_t ka = smem_u32(sm.k[nst]);
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + nst * 128, kdesc(qa, kk), kdesc(ka, kk), id_ss, kk > 0);
+          tc_commit(smem_u32(&sm.s_full[nst]));
+        }
+        const uint32_t kt = smem_u32(sm.k[st]);
+        if (!(ok = mbar_wait(smem_u32(&sm.ds_a[b]), (it >> 1) & 1, abort, status))) break;
+        tc_fence_after();
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ts(tmem + 384, tmem + b * 128 + kk * 8, mndesc(kt, kk), id_ts, (it > 0 || kk > 0) ? 1u : 0u);
+        if (!(ok = mbar_wait(smem_u32(&sm.ds_b[b]), (it >> 1) & 1, abort, status))) break;
+        tc_fence_after();
+        for (int kk = 4; kk < 8; ++kk) mma_ts(tmem + 384, tmem + b * 128 + kk * 8, mndesc(kt, kk), id_ts, 1u);
+        tc_commit(smem_u32(&sm.kv_empty[st]));
+        if (it + 1 < cnt) {
+          const uint32_t va = smem_u32(sm.v[(it + 1) & 1]);
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + 256, kdesc(da, kk), kdesc(va, kk), id_ss, kk > 0);
+          tc_commit(smem_u32(&sm.dp_full));
+        }
+      }
+      tc_commit(smem_u32(&sm.acc_done));
+      tc_commit(smem_u32(&sm.mma_done));
+      drain_wait(smem_u32(&sm.mma_done), 0);
+    }
+  } else if (warp >= 2) {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int row = i * kB + r;
+    const float l2 = L2[(size_t)h * npad + row];
+    const float dr = Dp[(size_t)h * npad + row];
+    bool ok = true;
+    for (int it = 0; it < cnt; ++it) {
+      const int b = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[b]), (it >> 1) & 1, abort, status) &&
+                                       mbar_wait(smem_u32(&sm.dp_full), it & 1, abort, status));
+      if (!ok) break;
+      tc_fence_after();
+      int j = lst[it];
+      const int len = (j >= 0 && j < nb) ? min(kB, N - j * kB) : 0;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t sr[32], pr[32];
+        tmem_ld32(lane_base + b * 128 + c4 * 32, sr);
+        tmem_ld32(lane_base + 256 + c4 * 32, pr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(pr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int c = c4 * 32 + 2 * x;
+          const float p0 = c < len ? fast_exp2(fmaf(__uint_as_float(sr[2 * x]), kSl2, -l2)) : 0.f;
+          const float p1 = c + 1 < len ? fast_exp2(fmaf(__uint_as_float(sr[2 * x + 1]), kSl2, -l2)) : 0.f;
+          pk[x] = pack_bf16x2(p0 * (__uint_as_float(pr[2 * x]) - dr), p1 * (__uint_as_float(pr[2 * x + 1]) - dr));
+        }
+        tmem_st16(lane_base + b * 128 + c4 * 16, pk);
+        if (c4 == 1 || c4 == 3) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(c4 == 1 ? &sm.ds_a[b] : &sm.ds_b[b]));
+        }
+      }
+    }
+    __nv_bfloat16* out = dq + (int64_t)row * ld + (int64_t)h * kD;
+    if (ok && cnt > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_done), 0, abort, status));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t rr[32];
+          tmem_load_row32(lane_base + 384 + c4 * 32, rr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            pk[x] = pack_bf16x2(__uint_as_float(rr[2 * x]) * kScale, __uint_as_float(rr[2 * x + 1]) * kScale);
+          if (row < N) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c4 * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+          }
+        }
+      }
+    } else if (cnt == 0 && row < N) {
+      uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) dst[x] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------- dK dV
+struct QdoStage {
+  uint8_t q[kTile];
+  uint8_t dO[kTile];
+};
+struct DkdvSmem {
+  uint8_t k[kTile];
+  uint8_t v[kTile];
+  QdoStage st[2];
+  float l2[2][kB];  // lse * log2(e) of the stage's query rows
+  float dr[2][kB];  // D of the stage's query rows
+  uint64_t kv_full;
+  uint64_t qdo_full[2], qdo_empty[2];
+  uint64_t sdp_full, half_a, half_b;
+  uint64_t acc_done, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kDkdvSmemBytes = sizeof(DkdvSmem) + 1024;
+static_assert(kDkdvSmemBytes <= 232448, "shared memory budget");
+static_assert(sizeof(QdoStage) % 1024 == 0, "stages keep 1024-byte alignment for the swizzled tiles");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bsa_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                       const float* __restrict__ L2, const float* __restrict__ Dp, int npad,
+                       __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int64_t ld, int N,
+                       const int32_t* __restrict__ tcounts, const int32_t* __restrict__ tidx, int nb,
+                       uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  DkdvSmem& sm = *reinterpret_cast<DkdvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x;
+  const int h = item / nb, j = item - h * nb;
+  const int cnt = tcounts[item];
+  const int32_t* lst = tidx + (size_t)item * nb;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.kv_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&sm.qdo_full[s]), 1);
+      mbar_init(smem_u32(&sm.qdo_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&sm.sdp_full), 1);
+    mbar_init(smem_u32(&sm.half_a), 4);
+    mbar_init(smem_u32(&sm.half_b), 4);
+    mbar_init(smem_u32(&sm.acc_done), 1);
+    mbar_init(smem_u32(&sm.mma_done), 1);
+    sm.abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;  // S^T [0,128) dP^T [128,256) dV [256,384) dK [384,512)
+  volatile int* abort = &sm.abort;
+
+  if (warp == 0) {
+    if (lane == 0 && cnt > 0) {
+      const uint32_t kvb = smem_u32(&sm.kv_full);
+      mbar_arrive_expect_tx(kvb, 2 * kTile);
+      tma_load_2d(smem_u32(sm.k), &tmk, h * kD, j * kB, kvb);
+      tma_load_2d(smem_u32(sm.k) + kHalf, &tmk, h * kD + 64, j * kB, kvb);
+      tma_load_2d(smem_u32(sm.v), &tmv, h * kD, j * kB, kvb);
+      tma_load_2d(smem_u32(sm.v) + kHalf, &tmv, h * kD + 64, j * kB, kvb);
+      int armed[2] = {0, 0};
+      for (int it = 0; it < cnt; ++it) {
+        const int s = it & 1;
+        if (it >= 2 && !mbar_wait(smem_u32(&sm.qdo_empty[s]), ((it >> 1) - 1) & 1, abort, status)) break;
+        const int i = lst[it];
+        QdoStage& g = sm.st[s];
+        const uint32_t bar = smem_u32(&sm.qdo_full[s]);
+        mbar_arrive_expect_tx(bar, 2 * kTile + 2 * kB * 4);
+        tma_load_2d(smem_u32(g.q), &tmq, h * kD, i * kB, bar);
+        tma_load_2d(smem_u32(g.q) + kHalf, &tmq, h * kD + 64, i * kB, bar);
+        tma_load_2d(smem_u32(g.dO), &tmdo, h * kD, i * kB, bar);
+        tma_load_2d(smem_u32(g.dO) + kHalf, &tmdo, h * kD + 64, i * kB, bar);
+        bulk_load(smem_u32(sm.l2[s]), L2 + (size_t)h * npad + (size_t)i * kB, kB * 4, bar);
+        bulk_load(smem_u32(sm.dr[s]), Dp + (size_t)h * npad + (size_t)i * kB, kB * 4, bar);
+        ++armed[s];
+      }
+      if (*abort) {
+        drain_wait(kvb, 0);
+        for (int s = 0; s < 2; ++s)
+          if (armed[s]) drain_wait(smem_u32(&sm.qdo_full[s]), (armed[s] - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && cnt > 0) {
+      constexpr uint32_t id_ss = idesc_bf16_f32(kB, kB, false, false);
+      constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
+      bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, abort, status);
+      for (int it = 0; ok && it < cnt; ++it) {
+        const int s = it & 1;
+        if (!(ok = mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status))) break;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(sm.st[s].q), da = smem_u32(sm.st[s].dO);
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, kdesc(ka, kk), kdesc(qa, kk), id_ss, kk > 0);
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + 128, kdesc(va, kk), kdesc(da, kk), id_ss, kk > 0);
+        tc_commit(smem_u32(&sm.sdp_full));
+        if (!(ok = mbar_wait(smem_u32(&sm.half_a), it & 1, abort, status))) break;
+        tc_fence_after();
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          mma_ts(tmem + 256, tmem + kk * 8, mndesc(da, kk), id_ts, acc);
+          mma_ts(tmem + 384, tmem + 128 + kk * 8, mndesc(qa, kk), id_ts, acc);
+        }
+        if (!(ok = mbar_wait(smem_u32(&sm.half_b), it & 1, abort, status))) break;
+        tc_fence_after();
+        for (int kk = 4; kk < 8; ++kk) {
+          mma_ts(tmem + 256, tmem + kk * 8, mndesc(da, kk), id_ts, 1u);
+          mma_ts(tmem + 384, tmem + 128 + kk * 8, mndesc(qa, kk), id_ts, 1u);
+        }
+        tc_commit(smem_u32(&sm.qdo_empty[s]));
+      }
+      tc_commit(smem_u32(&sm.acc_done));
+      tc_commit(smem_u32(&sm.mma_done));
+      drain_wait(smem_u32(&sm.mma_done), 0);
+    }
+  } else if (warp >= 2) {
+    const int quarter = warp & 3;
+    const int c = quarter * 32 + lane;  // key row of block j = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    bool ok = true;
+    for (int it = 0; it < cnt; ++it) {
+      const int s = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status) &&
+                                       mbar_wait(smem_u32(&sm.sdp_full), it & 1, abort, status));
+      if (!ok) break;
+      tc_fence_after();
+      const float* l2 = sm.l2[s];
+      const float* dr = sm.dr[s];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t sr[32], pr[32];
+        tmem_ld32(lane_base + c4 * 32, sr);
+        tmem_ld32(lane_base + 128 + c4 * 32, pr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(pr);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int q0 = c4 * 32 + 2 * x;
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * x]), kSl2, -l2[q0]));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * x + 1]), kSl2, -l2[q0 + 1]));
+          pp[x] = pack_bf16x2(p0, p1);
+          dd[x] = pack_bf16x2(p0 * (__uint_as_float(pr[2 * x]) - dr[q0]), p1 * (__uint_as_float(pr[2 * x + 1]) - dr[q0 + 1]));
+        }
+        tmem_st16(lane_base + c4 * 16, pp);
+        tmem_st16(lane_base + 128 + c4 * 16, dd);
+        if (c4 == 1 || c4 == 3) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(c4 == 1 ? &sm.half_a : &sm.half_b));
+        }
+      }
+    }
+    const int col = j * kB + c;
+    __nv_bfloat16* dk_row = dk + (int64_t)col * ld + (int64_t)h * kD;
+    __nv_bfloat16* dv_row = dv + (int64_t)col * ld + (int64_t)h * kD;
+    if (ok && cnt > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_done), 0, abort, status));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          __nv_bfloat16* out = half ? dk_row : dv_row;
+          const float sc = half ? kScale : 1.f;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t rr[32];
+            tmem_load_row32(lane_base + 256 + half * 128 + c4 * 32, rr);
+            uint32_t pk[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+              pk[x] = pack_bf16x2(__uint_as_float(rr[2 * x]) * sc, __uint_as_float(rr[2 * x + 1]) * sc);
+            if (col < N) {
+              uint4* dst = reinterpret_cast<uint4*>(out + c4 * 32);
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+            }
+          }
+        }
+      }
+    } else if (cnt == 0 && col < N) {
+      uint4* a = reinterpret_cast<uint4*>(dk_row);
+      uint4* b = reinterpret_cast<uint4*>(dv_row);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) a[x] = b[x] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+size_t bwd_tc_rowstats_bytes(int Hh, int nb) { return (size_t)2 * Hh * nb * kB * sizeof(float); }
+
+cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                              const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,
+                              const int32_t* idx, int nb, void* dq, void* dk, void* dv, const int32_t* tcounts,
+                              const int32_t* tidx, float* rowstats, cudaStream_t st, uint32_t* status) {
+  const int npad = nb * kB;
+  float* L2 = rowstats;
+  float* Dp = rowstats + (size_t)Hh * npad;
+  const int64_t threads = (int64_t)Hh * npad * 32;
+  bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, ld, N, Hh, npad, L2, Dp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv, mdo;
+  const uint64_t inner = (uint64_t)Hh * kD, row_bytes = (uint64_t)ld * 2;
+  if (!tensor_map_2d_bf16(&mq, q, inner, N, row_bytes, 64, kB) ||
+      !tensor_map_2d_bf16(&mk, k, inner, N, row_bytes, 64, kB) ||
+      !tensor_map_2d_bf16(&mv, v, inner, N, row_bytes, 64, kB) ||
+      !tensor_map_2d_bf16(&mdo, dO, inner, N, row_bytes, 64, kB))
+    return cudaErrorInvalidValue;
+  if ((e = cudaFuncSetAttribute(bsa_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kDqSmemBytes)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bsa_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kDkdvSmemBytes)) != cudaSuccess)
+    return e;
+  bsa_dq_tc_kernel<<<(unsigned)Hh * nb, kThreads, kDqSmemBytes, st>>>(
+      mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dq), ld, N, counts, idx, nb, status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bsa_dkdv_tc_kernel<<<(unsigned)Hh * nb, kThreads, kDkdvSmemBytes, st>>>(
+      mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), ld, N,
+      tcounts, tidx, nb, status);
+  return cudaGetLastError();
+}
+
+}  // namespace prism

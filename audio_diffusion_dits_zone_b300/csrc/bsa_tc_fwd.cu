@@ -91,30 +91,6 @@ struct FwdSmem {
 constexpr size_t kFwdSmemBytes = sizeof(FwdSmem) + 1024;
 static_assert(kFwdSmemBytes <= 232448, "shared memory budget");
 
-__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
-  asm volatile(""
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
-                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
-}
-
-// Load 32 TMEM columns of this thread's lane and wait for them.
-__device__ __forceinline__ void tmem_load_row32(uint32_t taddr, uint32_t (&r)[32]) {
-  tmem_ld32(taddr, r);
-  tmem_wait_ld();
-  reg_fence(r);
-}
-
-// Drain wait used on the way out: ignores the abort flag, bounded in time.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) return;
-  }
-}
-
 __device__ __forceinline__ int block_of(const int32_t* lst, int it, int nb, bool& ok) {
   const int j = lst[it];
   ok = (j >= 0 && j < nb);

@@ -61,10 +61,11 @@ cudaError_t row_dot_launch(const void* o, const void* dO, int dtype, int64_t ld,
 cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
                               const int32_t* counts, const int32_t* idx, int nb, void* o, float* lse,
                               cudaStream_t st, uint32_t* status);
+size_t bwd_tc_rowstats_bytes(int Hh, int nb);
 cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,
                               const int32_t* idx, int nb, void* dq, void* dk, void* dv, const int32_t* tcounts,
-                              const int32_t* tidx, float* Drow, cudaStream_t st, uint32_t* status);
+                              const int32_t* tidx, float* rowstats, cudaStream_t st, uint32_t* status);
 
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,

@@ -219,17 +219,23 @@ int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk, const
   int rc = check_attention_args(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb);
   if (rc != PRISM_OK) return rc;
   const size_t lists = prism::lists_ws_bytes(Hh, nb);
-  const size_t drow = ((size_t)Hh * N * sizeof(float) + 255) & ~(size_t)255;
-  if (ws_query(ws, ws_bytes, ws_round(lists + drow), &rc)) return rc;
+  const bool tc = use_tc(dtype, d, B, ld, {q_blk, k_blk, v_blk, o_blk, do_blk, dq, dk, dv});
+  const size_t rows = tc ? prism::bwd_tc_rowstats_bytes(Hh, nb) : (size_t)Hh * N * sizeof(float);
+  if (ws_query(ws, ws_bytes, ws_round(lists + ((rows + 255) & ~(size_t)255)), &rc)) return rc;
   if (!o_blk || !do_blk || !lse || !dq || !dk || !dv) return fail(PRISM_EINVAL, "NULL pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* tcounts = nullptr;
   int32_t* tidx = nullptr;
-  float* Drow = reinterpret_cast<float*>(static_cast<char*>(ws) + lists);
+  float* rowstats = reinterpret_cast<float*>(static_cast<char*>(ws) + lists);
   cudaError_t e = prism::transpose_lists_launch(counts, idx, Hh, nb, ws, &tcounts, &tidx, st, status_ptr());
-  if (e == cudaSuccess)
-    e = prism::bsa_bwd_simt_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, dtype, ld, N, Hh, d, B, counts, idx,
-                                   nb, dq, dk, dv, tcounts, tidx, Drow, st, status_ptr());
+  if (e == cudaSuccess) {
+    if (tc)
+      e = prism::bsa_bwd_tc_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, ld, N, Hh, counts, idx, nb, dq, dk, dv,
+                                   tcounts, tidx, rowstats, st, status_ptr());
+    else
+      e = prism::bsa_bwd_simt_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, dtype, ld, N, Hh, d, B, counts, idx,
+                                     nb, dq, dk, dv, tcounts, tidx, rowstats, st, status_ptr());
+  }
   return e == cudaSuccess ? (launched(5), ok()) : cuda_fail(e, "prism_bsa_bwd");
 }
 
@@ -256,7 +262,7 @@ uint64_t prism_launch_count(void) { return g_launches.load(std::memory_order_rel
 
 const char* prism_build_info(void) {
   return "libprism 0.1 | sm_103a | bsa_fwd: tcgen05+TMA for bf16 d=128 B=128, CUDA cores otherwise | "
-         "bsa_bwd: CUDA cores | select: nb <= 4096 | zone: <= 6400 tokens per zone";
+         "bsa_bwd: tcgen05+TMA for bf16 d=128 B=128, CUDA cores otherwise | select: nb <= 4096 | zone: <= 6400 tokens per zone";
 }
 
 int prism_selftest_umma(const void* a, const void* b, float* out_s, float* out_o, int32_t variant, void* stream) {

@@ -248,3 +248,49 @@ def test_bad_block_index_is_skipped_and_flagged():
                            128)
     attn_close(o.float().cpu().numpy(), oO, what="O with a skipped index")
     assert w == 2   # PRISM_DEV_BAD_INDEX
+
+
+def test_bsa_bwd_dense_matches_sdpa_autograd():
+    # every block kept: the tensor-core backward must reproduce the gradients of dense
+    # softmax attention, taken by torch autograd through SDPA in fp64
+    wl = small_workload((1, 1, 1100), 2, 128, "bf16", 128)
+    Q, K, V = qkv(wl)
+    dO = np.stack(synth.gen_heads(wl, synth.DO_ID, range(2)), axis=1)
+    nb, N = wl.nb, wl.N
+    counts = np.full((2, nb), nb, np.int32)
+    idx = np.broadcast_to(np.arange(nb, dtype=np.int32), (2, nb, nb)).copy()
+    q, k, v, g = (to_dev(x, torch.bfloat16) for x in (Q, K, V, dO))
+    c, ix = torch.from_numpy(counts).to(dev), torch.from_numpy(idx).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(2, N, device=dev)
+    P.prism_bsa_fwd(q, k, v, 128, c, ix, o, lse)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    P.prism_bsa_bwd(q, k, v, o, g, lse, 128, c, ix, dq, dk, dv)
+    assert P.status_check() == 0
+    tq, tk, tv = (torch.from_numpy(x.astype(np.float64)).permute(1, 0, 2)[None].requires_grad_() for x in (Q, K, V))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv)
+    ref.backward(torch.from_numpy(dO.astype(np.float64)).permute(1, 0, 2)[None])
+    for got, t, name in ((dq, tq, "dQ"), (dk, tk, "dK"), (dv, tv, "dV")):
+        attn_close(got.float().cpu().numpy(), t.grad[0].permute(1, 0, 2).numpy(), what=name)
+
+
+@pytest.mark.parametrize("N,heads,seed", [(2048, 3, 1), (1500, 2, 2)])
+def test_bsa_bwd_tensor_core_random_lists(N, heads, seed):
+    wl = small_workload((1, 1, N), heads, 128, "bf16", 128, cid=70 + seed)
+    Q, K, V = qkv(wl)
+    dO = np.stack(synth.gen_heads(wl, synth.DO_ID, range(heads)), axis=1)
+    nb = wl.nb
+    counts, idx = lists_for(nb, heads, seed=100 + seed)
+    f64 = lambda x: x.astype(np.float64)  # noqa: E731
+    oO, oL = po.bsa_forward(f64(Q), f64(K), f64(V), counts, idx, 128)
+    O_in = synth.to_bf16(oO.astype(np.float32))
+    L_in = oL.astype(np.float32)
+    dQ, dK, dV = po.bsa_backward(f64(Q), f64(K), f64(V), f64(O_in), f64(dO), f64(L_in), counts, idx, 128)
+    q, k, v, o, g = (to_dev(x, torch.bfloat16) for x in (Q, K, V, O_in, dO))
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    P.prism_bsa_bwd(q, k, v, o, g, torch.from_numpy(L_in).to(dev), 128, torch.from_numpy(counts).to(dev),
+                    torch.from_numpy(idx).to(dev), dq, dk, dv)
+    assert P.status_check() == 0
+    attn_close(dq.float().cpu().numpy(), dQ, what="dQ")
+    attn_close(dk.float().cpu().numpy(), dK, what="dK")
+    attn_close(dv.float().cpu().numpy(), dV, what="dV")
