@@ -100,9 +100,13 @@ cudaError_t transpose_lists_launch(const int32_t* counts, const int32_t* idx, in
   *tidx = reinterpret_cast<int32_t*>(p);
   cudaError_t e = cudaMemsetAsync(bits, 0, (size_t)Hh * nb * words * 4, st);
   if (e != cudaSuccess) return e;
-  set_bits_kernel<<<Hh * nb, 128, 0, st>>>(counts, idx, Hh, nb, bits, status);
+  {
+    HookScope hs("lists_set_bits", st);
+    set_bits_kernel<<<Hh * nb, 128, 0, st>>>(counts, idx, Hh, nb, bits, status);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t threads = (int64_t)Hh * nb * 32;
+  HookScope hs("lists_emit", st);
   emit_lists_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(bits, Hh, nb, *tcounts, *tidx);
   return cudaGetLastError();
 }
@@ -111,6 +115,7 @@ cudaError_t row_dot_launch(const void* o, const void* dO, int dtype, int64_t ld,
                            cudaStream_t st) {
   const int64_t threads = (int64_t)N * Hh * 32;
   const unsigned blocks = (unsigned)((threads + 255) / 256);
+  HookScope hs("row_dot", st);
   if (dtype == PRISM_BF16)
     row_dot_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(o),
                                                           static_cast<const __nv_bfloat16*>(dO), ld, N, Hh, d, Drow);

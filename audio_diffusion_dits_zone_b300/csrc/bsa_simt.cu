@@ -237,6 +237,7 @@ cudaError_t fwd_t(const void* q, const void* k, const void* v, int64_t ld, int N
   const size_t smem = (size_t)2 * B * D * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  HookScope hs("bsa_fwd_simt", st);
   kern<<<dim3(nb, Hh), B * TPR, smem, st>>>(static_cast<const T*>(q), static_cast<const T*>(k),
                                              static_cast<const T*>(v), ld, N, B, counts, idx, nb,
                                              static_cast<T*>(o), lse, status);
@@ -256,10 +257,14 @@ cudaError_t bwd_t(const void* q, const void* k, const void* v, const void* dO, c
   if (e != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_k)) != cudaSuccess)
     return e;
+  {
+  HookScope hs("bsa_dq_simt", st);
   kq<<<dim3(nb, Hh), B * TPR_Q, smem_q, st>>>(static_cast<const T*>(q), static_cast<const T*>(k),
                                                static_cast<const T*>(v), static_cast<const T*>(dO), lse, Drow, ld,
                                                N, B, counts, idx, nb, static_cast<T*>(dq));
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  HookScope hs("bsa_dkdv_simt", st);
   const int splits = B > kRowsPerCta ? B / kRowsPerCta : 1;
   kk<<<dim3(nb * splits, Hh), (B / splits) * TPR_K, smem_k, st>>>(static_cast<const T*>(q), static_cast<const T*>(k),
                                                static_cast<const T*>(v), static_cast<const T*>(dO), lse, Drow, ld,

@@ -495,8 +495,11 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
   float* L2 = rowstats;
   float* Dp = rowstats + (size_t)Hh * npad;
   const int64_t threads = (int64_t)Hh * npad * 32;
-  bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, ld, N, Hh, npad, L2, Dp);
+  {
+    HookScope hs("bwd_prep", st);
+    bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, ld, N, Hh, npad, L2, Dp);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo;
@@ -512,9 +515,13 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
   if ((e = cudaFuncSetAttribute(bsa_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kDkdvSmemBytes)) != cudaSuccess)
     return e;
-  bsa_dq_tc_kernel<<<(unsigned)Hh * nb, kThreads, kDqSmemBytes, st>>>(
-      mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dq), ld, N, counts, idx, nb, status);
+  {
+    HookScope hs("bsa_dq_tc", st);
+    bsa_dq_tc_kernel<<<(unsigned)Hh * nb, kThreads, kDqSmemBytes, st>>>(
+        mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dq), ld, N, counts, idx, nb, status);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  HookScope hs("bsa_dkdv_tc", st);
   bsa_dkdv_tc_kernel<<<(unsigned)Hh * nb, kThreads, kDkdvSmemBytes, st>>>(
       mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), ld, N,
       tcounts, tidx, nb, status);

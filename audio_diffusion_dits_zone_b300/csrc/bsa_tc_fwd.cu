@@ -451,6 +451,7 @@ cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64
   cudaError_t e = cudaFuncSetAttribute(bsa_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kFwdSmemBytes);
   if (e != cudaSuccess) return e;
+  HookScope hs("bsa_fwd_tc", st);
   bsa_fwd_tc_kernel<<<(unsigned)Hh * nb, kThreads, kFwdSmemBytes, st>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, ld, N, counts, idx, nb, status);
   return cudaGetLastError();

@@ -10,6 +10,16 @@ namespace prism {
 // Record `msg` as the calling thread's last error (prism_last_error) and return `code`.
 int report_error(int code, const char* msg);
 
+// Launch observer (prism_set_launch_hook): called right before (phase 0) and right
+// after (phase 1) a kernel is enqueued on `st`.
+void launch_hook(const char* kernel, cudaStream_t st, int phase);
+struct HookScope {
+  const char* name;
+  cudaStream_t st;
+  HookScope(const char* n, cudaStream_t s) : name(n), st(s) { launch_hook(name, st, 0); }
+  ~HookScope() { launch_hook(name, st, 1); }
+};
+
 struct ZoneGeom {
   int T, H, W;      // token grid
   int zt, zh, zw;   // zone extents

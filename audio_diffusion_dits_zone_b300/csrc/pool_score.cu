@@ -183,6 +183,7 @@ cudaError_t launch_pool(const void* q, const void* k, const void* v, int64_t ld,
                         int d, int B, void* qb, void* kb, void* vb, int64_t ldb, float* qbar, float* kbar,
                         cudaStream_t st, uint32_t* status) {
   const int nb = (N + B - 1) / B;
+  HookScope hs("pool_gather", st);
   pool_gather_kernel<T, VW><<<nb, kPoolThreads, (size_t)B * sizeof(int32_t), st>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), ld, perm, N, Hh, d, B,
       static_cast<T*>(qb), static_cast<T*>(kb), static_cast<T*>(vb), ldb, qbar, kbar, nb, status);
@@ -211,6 +212,7 @@ cudaError_t pool_launch(const void* q, const void* k, const void* v, int dtype, 
 cudaError_t scores_launch(const float* qbar, const float* kbar, int Hh, int nb, int d, float* scores,
                           cudaStream_t st) {
   const dim3 grid((nb + kTile - 1) / kTile, (nb + kTile - 1) / kTile, Hh);
+  HookScope hs("scores", st);
   scores_kernel<<<grid, 256, 0, st>>>(qbar, kbar, nb, d, 1.0f / sqrtf((float)d), scores);
   return cudaGetLastError();
 }

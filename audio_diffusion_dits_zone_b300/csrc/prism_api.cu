@@ -119,6 +119,16 @@ bool use_tc(int32_t dtype, int32_t d, int32_t B, int64_t ld, std::initializer_li
 
 namespace prism {
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+namespace {
+std::atomic<prism_launch_hook_fn> g_hook{nullptr};
+std::atomic<void*> g_hook_user{nullptr};
+}  // namespace
+
+void launch_hook(const char* kernel, cudaStream_t st, int phase) {
+  prism_launch_hook_fn f = g_hook.load(std::memory_order_acquire);
+  if (f) f(kernel, st, phase, g_hook_user.load(std::memory_order_relaxed));
+}
 }  // namespace prism
 
 extern "C" {
@@ -259,6 +269,11 @@ int prism_status_check(void* stream, uint32_t* word) {
 const char* prism_last_error(void) { return g_last_error.c_str(); }
 
 uint64_t prism_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void prism_set_launch_hook(prism_launch_hook_fn fn, void* user) {
+  prism::g_hook_user.store(user, std::memory_order_relaxed);
+  prism::g_hook.store(fn, std::memory_order_release);
+}
 
 const char* prism_build_info(void) {
   return "libprism 0.1 | sm_103a | bsa_fwd: tcgen05+TMA for bf16 d=128 B=128, CUDA cores otherwise | "

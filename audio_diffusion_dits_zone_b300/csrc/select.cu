@@ -139,6 +139,7 @@ cudaError_t select_launch(const float* scores, int Hh, int nb, int k_top, float 
   int P = 1;
   while (P < nb) P <<= 1;
   if (P < 2) P = 2;
+  HookScope hs("select", st);
   select_kernel<<<(unsigned)Hh * nb, kSelThreads, 0, st>>>(scores, nb, P, k_top, tau, counts, idx);
   return cudaGetLastError();
 }

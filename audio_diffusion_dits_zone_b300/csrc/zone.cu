@@ -316,11 +316,13 @@ cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const fl
       auto k = zone_partial_kernel<__nv_bfloat16, 8>;
       if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
+      HookScope hs("zone_partial", st);
       k<<<grid, kZoneThreads, smem, st>>>(static_cast<const __nv_bfloat16*>(feat), ld, C, g, ch, part);
     } else {
       auto k = zone_partial_kernel<__nv_bfloat16, 1>;
       if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
+      HookScope hs("zone_partial", st);
       k<<<grid, kZoneThreads, smem, st>>>(static_cast<const __nv_bfloat16*>(feat), ld, C, g, ch, part);
     }
   } else {
@@ -329,23 +331,34 @@ cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const fl
       auto k = zone_partial_kernel<float, 4>;
       if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
+      HookScope hs("zone_partial", st);
       k<<<grid, kZoneThreads, smem, st>>>(static_cast<const float*>(feat), ld, C, g, ch, part);
     } else {
       auto k = zone_partial_kernel<float, 1>;
       if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
+      HookScope hs("zone_partial", st);
       k<<<grid, kZoneThreads, smem, st>>>(static_cast<const float*>(feat), ld, C, g, ch, part);
     }
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+  HookScope hs("zone_finalize", st);
   zone_finalize_kernel<<<g.Z, kZoneThreads, (size_t)g.max_tokens * sizeof(float), st>>>(part, nchunks, a2v, g, C,
                                                                                         stats);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  zone_choose_kernel<<<1, 1024, 0, st>>>(stats, g.Z, shapes, zone_shape);
+  {
+    HookScope hs("zone_choose", st);
+    zone_choose_kernel<<<1, 1024, 0, st>>>(stats, g.Z, shapes, zone_shape);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t N = (int64_t)g.T * g.H * g.W;
   const int blocks = (int)std::min<int64_t>((N + 255) / 256, 148 * 16);
-  zone_perm_kernel<<<blocks, 256, 0, st>>>(g, zone_shape, shapes, perm);
+  {
+    HookScope hs("zone_perm", st);
+    zone_perm_kernel<<<blocks, 256, 0, st>>>(g, zone_shape, shapes, perm);
+  }
   return cudaGetLastError();
 }
 

@@ -36,7 +36,9 @@ _SIGS = {
     "prism_launch_count": [],
     "prism_build_info": [],
     "prism_selftest_umma": [_P, _P, _P, _P, _I32, _P],
+    "prism_set_launch_hook": [_P, _P],
 }
+LAUNCH_HOOK = ctypes.CFUNCTYPE(None, ctypes.c_char_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p)
 _lib = None
 
 
@@ -60,6 +62,9 @@ def lib() -> ctypes.CDLL:
             f.restype = ctypes.c_char_p if name in ("prism_last_error", "prism_build_info") else ctypes.c_int
             if name == "prism_launch_count":
                 f.restype = ctypes.c_uint64
+            if name == "prism_set_launch_hook":
+                f.argtypes = [LAUNCH_HOOK, ctypes.c_void_p]
+                f.restype = None
         _lib = L
     return _lib
 
@@ -102,6 +107,49 @@ def _ld(t):
 def launch_count() -> int:
     """Kernels the library has enqueued so far."""
     return int(lib().prism_launch_count())
+
+
+def prism_set_launch_hook(fn):
+    """Install a Python observer fn(kernel_name: str, stream_ptr: int, phase: int) called
+    right before (0) and after (1) each kernel launch; None removes it.  Returns the
+    ctypes callback object, which must be kept alive while installed."""
+    if fn is None:
+        lib().prism_set_launch_hook(LAUNCH_HOOK(), None)
+        return None
+    cb = LAUNCH_HOOK(lambda name, stream, phase, user: fn(name.decode(), stream or 0, phase))
+    lib().prism_set_launch_hook(cb, None)
+    return cb
+
+
+class KernelTimer:
+    """CUDA events recorded on the launching stream around every library kernel."""
+
+    def __init__(self):
+        self.records = []
+        self._cb = None
+
+    def _on_launch(self, name, stream, phase):
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(torch.cuda.ExternalStream(stream) if stream else torch.cuda.current_stream())
+        self.records.append((name, phase, ev))
+
+    def __enter__(self):
+        self._cb = prism_set_launch_hook(self._on_launch)
+        return self
+
+    def __exit__(self, *exc):
+        prism_set_launch_hook(None)
+        self._cb = None
+
+    def durations(self) -> dict:
+        """kernel name -> list of launch durations (ms); call after synchronising."""
+        out, open_ = {}, {}
+        for name, phase, ev in self.records:
+            if phase == 0:
+                open_[name] = ev
+            elif name in open_:
+                out.setdefault(name, []).append(open_.pop(name).elapsed_time(ev))
+        return out
 
 
 def build_info() -> str:

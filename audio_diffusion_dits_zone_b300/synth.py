@@ -87,6 +87,9 @@ WORKLOADS = {
     "train720p": Workload("train720p", 4, (21, 45, 80), 40, 128, "bf16", (3, 9, 16), 128,
                           SHAPES_128, 0.80, 0.20, 1, 3.0, (44, 42, 42), "fwd+bwd",
                           sweep=(0.0, 0.75, 0.80, 0.85, 0.93)),
+    # the 720p training layer with 4 heads: a small case of the same kernels for profiling
+    "720p-4h": Workload("720p-4h", 5, (21, 45, 80), 4, 128, "bf16", (3, 9, 16), 128, SHAPES_128,
+                        0.80, 0.20, 1, 3.0, (44, 42, 42), "fwd+bwd"),
 }
 
 

@@ -136,13 +136,14 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         layer.step()
     torch.cuda.synchronize()
-    # ---------------- timed region: K steps, events around every call on the launching stream
+    # ---------------- timed region: K steps; events around every call and every kernel,
+    # all recorded on the launching stream (torch's current stream)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
     launches0 = P.launch_count()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(local_rank) as clk, P.KernelTimer() as kt:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
@@ -164,32 +165,56 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError("device status word set during the timed region")
     per_call = {n: statistics.mean(ev[s][c].elapsed_time(ev[s][c + 1]) for s in range(args.steps))
                 for c, n in enumerate(names)}
+    kdur = kt.durations()
+    per_kernel = {n: {"ms_per_step": round(sum(v) / args.steps, 4), "launches_per_step": len(v) // args.steps,
+                      "ms_per_launch": round(statistics.mean(v), 4)} for n, v in kdur.items()}
     ms = elapsed_ms / args.steps
     pk = peaks()
     value = world * work / (ms * 1e-3) / 1e12
 
-    # dominant kernel: the call that takes the longest (both attention calls are tensor-bound)
-    dom = max(("bsa_fwd", "bsa_bwd"), key=lambda n: per_call[n])
-    dom_flops = fwd_fl if dom == "bsa_fwd" else bwd_fl
-    achieved = dom_flops / (per_call[dom] * 1e-3) / 1e12
+    # algorithmic work of each kernel per step: the matmul FLOPs it performs
+    # (tensor-bound kernels) or the bytes it must move (memory-bound kernels)
+    pairs = fwd_fl / (4.0 * wl.d)
+    C = wl.heads * wl.d
+    kept = int(layer.counts.sum().item())
+    algo = {
+        "bsa_fwd_tc": ("tensor", 4.0 * pairs * wl.d), "bsa_dq_tc": ("tensor", 6.0 * pairs * wl.d),
+        "bsa_dkdv_tc": ("tensor", 8.0 * pairs * wl.d),
+        "zone_partial": ("hbm", wl.N * C * 2.0),
+        "pool_gather": ("hbm", 6.0 * wl.N * C * 2 + 2.0 * wl.heads * wl.nb * wl.d * 4),
+        "scores": ("hbm", wl.heads * wl.nb ** 2 * 4.0 + 2.0 * wl.heads * wl.nb * wl.d * 4),
+        "select": ("hbm", wl.heads * wl.nb ** 2 * 4.0 + wl.heads * wl.nb * 4 + 4.0 * kept),
+        "bwd_prep": ("hbm", 2.0 * wl.N * C * 2 + wl.heads * wl.N * 4 + 2.0 * wl.heads * wl.nb * wl.block * 4),
+    }
+    for n, (bound, w) in algo.items():
+        if n in per_kernel:
+            t = per_kernel[n]["ms_per_step"] * 1e-3
+            if bound == "tensor":
+                per_kernel[n]["TFLOP/s"] = round(w / t / 1e12, 2)
+                per_kernel[n]["frac_bf16_sustained"] = round(w / t / 1e12 / pk["bf16_sustained"], 4)
+            else:
+                per_kernel[n]["GB/s"] = round(w / t / 1e9, 1)
+                per_kernel[n]["frac_hbm"] = round(w / t / 1e9 / pk["hbm_gbs"], 4)
+    dom = max(per_kernel, key=lambda n: per_kernel[n]["ms_per_step"])
+    bound, w = algo.get(dom, ("tensor", 0.0))
+    t_launch = per_kernel[dom]["ms_per_launch"] * 1e-3
+    w_launch = w / max(1, per_kernel[dom]["launches_per_step"])
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
             traffic = json.load(f).get(f"{wl.name}:{dom}")
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": pk["bf16_sustained"],
-                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sustained"], 4), "traffic": traffic,
-                "peak_note": f"bf16 dense, sustained ({pk['source']}); burst {pk['bf16']}",
-                "frac_of_burst": round(achieved / pk["bf16"], 4)}
-    hbm = {}
-    algo_bytes = {
-        "zone_shapes": wl.N * wl.heads * wl.d * 2 + wl.N * 4 + wl.N * 4,
-        "pool_score": 3 * wl.N * wl.heads * wl.d * 2 * 2 + 2 * wl.heads * wl.nb * wl.d * 4 + wl.heads * wl.nb ** 2 * 4,
-        "select": wl.heads * wl.nb ** 2 * 4 + wl.heads * wl.nb * 4 + 4 * int(layer.counts.sum().item()),
-    }
-    for n, b in algo_bytes.items():
-        gbs = b / (per_call[n] * 1e-3) / 1e9
-        hbm[n] = {"ms": round(per_call[n], 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+    if bound == "tensor":
+        achieved = w_launch / t_launch / 1e12
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": pk["bf16_sustained"],
+                    "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sustained"], 4), "traffic": traffic,
+                    "peak_note": f"bf16 dense, sustained ({pk['source']}); burst {pk['bf16']}",
+                    "frac_of_burst": round(achieved / pk["bf16"], 4),
+                    "algorithmic_per_launch": f"{w_launch:.4e} FLOP"}
+    else:
+        achieved = w_launch / t_launch / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic}
 
     # ---------------- end to end through the public API, host buffers
     e2e = run_e2e(layer, args, world)
@@ -203,9 +228,9 @@ def run_ours(args, rank, world, local_rank):
         "tflops_dense_equivalent": round((dense_f + dense_b) / (ms * 1e-3) / 1e12, 3),
         "pct_bf16_peak_executed": round(100 * work / (ms * 1e-3) / 1e12 / pk["bf16_sustained"], 2),
         "per_call_ms": {n: round(v, 4) for n, v in per_call.items()},
+        "per_kernel": per_kernel,
         "attention_tflops": {"bsa_fwd": round(fwd_fl / (per_call["bsa_fwd"] * 1e-3) / 1e12, 2),
                              "bsa_bwd": round(bwd_fl / (per_call["bsa_bwd"] * 1e-3) / 1e12, 2)},
-        "hbm_bound_calls": hbm,
         "kept_fraction": round(float(layer.counts.double().mean().item()) / wl.nb, 4),
         "roofline": roofline,
         "e2e": e2e,

@@ -205,6 +205,14 @@ const char* prism_last_error(void);
  * threads): a counter for measuring how many launches a step makes. */
 uint64_t prism_launch_count(void);
 
+/* Launch observer for profiling: when set, fn(kernel_name, stream, phase, user) is
+ * called on the calling host thread right before (phase 0) and right after (phase 1)
+ * each of the library's kernels is enqueued on `stream`, so a caller can record
+ * CUDA events around every kernel.  NULL removes it.  Changing it while other
+ * threads are inside library calls is not synchronised with those calls. */
+typedef void (*prism_launch_hook_fn)(const char* kernel, void* stream, int32_t phase, void* user);
+void prism_set_launch_hook(prism_launch_hook_fn fn, void* user);
+
 /* Build description: version, target architecture, compile-time limits. */
 const char* prism_build_info(void);
 
