@@ -437,7 +437,29 @@ __global__ void __launch_bounds__(128, 1) umma_selftest_kernel(const __grid_cons
   }
 }
 
+// Failure-path check: one CTA waits on an mbarrier that nothing ever arrives on, so
+// the bounded wait runs out after `limit_ns`, flags PRISM_DEV_TIMEOUT and the kernel
+// returns; it then writes `marker` so the host can see that it exited normally.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns, uint32_t* status, int* marker) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_limit(smem_u32(&bar), 0, &abort_flag, status, limit_ns);
+  __syncthreads();
+  if (threadIdx.x == 0) *marker = ok ? 1 : 2;
+}
+
 }  // namespace
+
+cudaError_t wait_timeout_selftest_launch(uint64_t limit_ns, int* marker, cudaStream_t st, uint32_t* status) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, status, marker);
+  return cudaGetLastError();
+}
 
 cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
                               const int32_t* counts, const int32_t* idx, int nb, void* o, float* lse,

@@ -61,23 +61,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase of parity `parity` of barrier `bar` has completed.  Gives up
-// after kWaitLimitNs or as soon as another thread of the CTA has raised `*abort`;
+// after `limit_ns` or as soon as another thread of the CTA has raised `*abort`;
 // on giving up it raises *abort, flags PRISM_DEV_TIMEOUT and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                uint32_t* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort = 1;
         flag_error(status, PRISM_DEV_TIMEOUT);
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status) {
+  return mbar_wait_limit(bar, parity, abort, status, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------------------ TMA

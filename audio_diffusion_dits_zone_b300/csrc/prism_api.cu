@@ -16,6 +16,7 @@
 namespace prism {
 cudaError_t umma_selftest_launch(const void* a, const void* b, float* out_s, float* out_o, int variant,
                                  cudaStream_t st, uint32_t* status);
+cudaError_t wait_timeout_selftest_launch(uint64_t limit_ns, int* marker, cudaStream_t st, uint32_t* status);
 }
 
 namespace {
@@ -285,6 +286,14 @@ int prism_selftest_umma(const void* a, const void* b, float* out_s, float* out_o
   cudaError_t e = prism::umma_selftest_launch(a, b, out_s, out_o, variant ? 1 : 0, static_cast<cudaStream_t>(stream),
                                               status_ptr());
   return e == cudaSuccess ? ok() : cuda_fail(e, "prism_selftest_umma");
+}
+
+int prism_selftest_wait_timeout(int64_t limit_ns, int32_t* marker, void* stream) {
+  if (!marker) return fail(PRISM_EINVAL, "marker must not be NULL");
+  if (limit_ns < 1000 || limit_ns > 1000000000) return fail(PRISM_EINVAL, "limit_ns must be in [1 us, 1 s]");
+  cudaError_t e = prism::wait_timeout_selftest_launch((uint64_t)limit_ns, marker, static_cast<cudaStream_t>(stream),
+                                                      status_ptr());
+  return e == cudaSuccess ? ok() : cuda_fail(e, "prism_selftest_wait_timeout");
 }
 
 }  // extern "C"

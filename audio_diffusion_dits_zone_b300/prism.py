@@ -36,6 +36,7 @@ _SIGS = {
     "prism_launch_count": [],
     "prism_build_info": [],
     "prism_selftest_umma": [_P, _P, _P, _P, _I32, _P],
+    "prism_selftest_wait_timeout": [_I64, _P, _P],
     "prism_set_launch_hook": [_P, _P],
 }
 LAUNCH_HOOK = ctypes.CFUNCTYPE(None, ctypes.c_char_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p)
@@ -257,3 +258,8 @@ def prism_bsa_bwd(q_blk, k_blk, v_blk, o_blk, do_blk, lse, B, counts, idx, dq, d
 
 def prism_selftest_umma(a, b, out_s, out_o, variant=0, stream=None):
     _check(lib().prism_selftest_umma(_ptr(a), _ptr(b), _ptr(out_s), _ptr(out_o), variant, _stream(stream)))
+
+
+def prism_selftest_wait_timeout(limit_ns, marker, stream=None):
+    """Run the bounded-wait failure check (see include/prism.h); marker: int32 device tensor."""
+    _check(lib().prism_selftest_wait_timeout(int(limit_ns), _ptr(marker), _stream(stream)))

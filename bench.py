@@ -53,6 +53,21 @@ def workload_config(wl, sparsity):
             "l2": "inputs larger than L2 (Q, K, V, dO 774 MB each); no flush"}
 
 
+# ------------------------------------------------------------ multi-rank
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (the job's time is its slowest rank's)."""
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(work_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank processes its own replica of the workload."""
+    return world * work_per_rank / seconds / 1e12
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
@@ -157,9 +172,7 @@ def run_ours(args, rank, world, local_rank):
     launches = P.launch_count() - launches0
     elapsed_ms = t0.elapsed_time(t1)
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dev)
         torch.distributed.barrier()
     if P.status_check() != 0:
         raise RuntimeError("device status word set during the timed region")
@@ -170,7 +183,7 @@ def run_ours(args, rank, world, local_rank):
                       "ms_per_launch": round(statistics.mean(v), 4)} for n, v in kdur.items()}
     ms = elapsed_ms / args.steps
     pk = peaks()
-    value = world * work / (ms * 1e-3) / 1e12
+    value = job_throughput(work, world, ms * 1e-3)
 
     # algorithmic work of each kernel per step: the matmul FLOPs it performs
     # (tensor-bound kernels) or the bytes it must move (memory-bound kernels)
@@ -272,9 +285,7 @@ def run_e2e(layer, args, world):
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     if world > 1:
-        t = torch.tensor([dt], device=layer.device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
+        dt = max_over_ranks(dt, layer.device)
     fwd_fl, bwd_fl, _, _ = layer.flops()
     return {"value": round(world * (fwd_fl + bwd_fl) / dt / 1e12, 3), "unit": UNIT, "ms_per_step": round(dt * 1e3, 3),
             "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in ins)),

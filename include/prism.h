@@ -226,6 +226,16 @@ const char* prism_build_info(void);
  */
 int prism_selftest_umma(const void* a, const void* b, float* out_s, float* out_o, int32_t variant, void* stream);
 
+/*
+ * Diagnostics: prism_selftest_wait_timeout launches one CTA that waits on an
+ * mbarrier nothing arrives on, with the same bounded wait the attention kernels
+ * use but a limit of limit_ns (1 us .. 1 s).  The wait gives up, the kernel sets
+ * PRISM_DEV_TIMEOUT in the status word and writes 2 to *marker (device int32) on
+ * its way out, so prism_status_check then returns PRISM_ETIMEOUT and the context
+ * stays usable.  Used to test the failure path without faulting or hanging a GPU.
+ */
+int prism_selftest_wait_timeout(int64_t limit_ns, int32_t* marker, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -294,3 +294,21 @@ def test_bsa_bwd_tensor_core_random_lists(N, heads, seed):
     attn_close(dq.float().cpu().numpy(), dQ, what="dQ")
     attn_close(dk.float().cpu().numpy(), dK, what="dK")
     attn_close(dv.float().cpu().numpy(), dV, what="dV")
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    # A wait that nothing satisfies gives up after 5 ms, flags the status word and the
+    # kernel exits normally; the next call on the same context still works.
+    marker = torch.zeros(1, dtype=torch.int32, device=dev)
+    P.prism_selftest_wait_timeout(5_000_000, marker)
+    w = P.status_check()
+    assert w & 1, f"status word 0x{w:x}"           # PRISM_DEV_TIMEOUT
+    assert int(marker.item()) == 2
+    assert P.status_check() == 0                     # the word was cleared
+    rng = np.random.default_rng(1)
+    a = synth.to_bf16(rng.normal(size=(128, 128)).astype(np.float32))
+    ta = to_dev(a, torch.bfloat16)
+    os_, oo = torch.zeros(128, 128, device=dev), torch.zeros(128, 128, device=dev)
+    P.prism_selftest_umma(ta, ta, os_, oo, 0)
+    assert P.status_check() == 0
+    np.testing.assert_allclose(os_.cpu().numpy(), a.astype(np.float64) @ a.astype(np.float64).T, atol=1e-3)
