@@ -219,28 +219,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       int j = lst[it];
       const int len = (j >= 0 && j < nb) ? min(kB, N - j * kB) : 0;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t sr[32], pr[32];
-        tmem_ld32(lane_base + b * 128 + c4 * 32, sr);
-        tmem_ld32(lane_base + 256 + c4 * 32, pr);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t s0[32], s1[32], d0[32], d1[32];
+        tmem_ld32(lane_base + b * 128 + half * 64, s0);
+        tmem_ld32(lane_base + b * 128 + half * 64 + 32, s1);
+        tmem_ld32(lane_base + 256 + half * 64, d0);
+        tmem_ld32(lane_base + 256 + half * 64 + 32, d1);
         tmem_wait_ld();
-        reg_fence(sr);
-        reg_fence(pr);
-        uint32_t pk[16];
+        reg_fence(s0);
+        reg_fence(s1);
+        reg_fence(d0);
+        reg_fence(d1);
+        if (len < kB) {  // short or skipped key block (warp-uniform): masked keys get P = 0
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int c = c4 * 32 + 2 * x;
-          const float p0 = c < len ? fast_exp2(fmaf(__uint_as_float(sr[2 * x]), kSl2, -l2)) : 0.f;
-          const float p1 = c + 1 < len ? fast_exp2(fmaf(__uint_as_float(sr[2 * x + 1]), kSl2, -l2)) : 0.f;
-          pk[x] = pack_bf16x2(p0 * (__uint_as_float(pr[2 * x]) - dr), p1 * (__uint_as_float(pr[2 * x + 1]) - dr));
+          for (int x = 0; x < 32; ++x) {
+            if (half * 64 + x >= len) s0[x] = __float_as_uint(-INFINITY);
+            if (half * 64 + 32 + x >= len) s1[x] = __float_as_uint(-INFINITY);
+          }
         }
-        tmem_st16(lane_base + b * 128 + c4 * 16, pk);
-        if (c4 == 1 || c4 == 3) {
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(c4 == 1 ? &sm.ds_a[b] : &sm.ds_b[b]));
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c4 = half * 2 + cc;
+          const uint32_t* sr = cc ? s1 : s0;
+          const uint32_t* pr = cc ? d1 : d0;
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * x]), kSl2, -l2));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * x + 1]), kSl2, -l2));
+            pk[x] = pack_bf16x2(p0 * (__uint_as_float(pr[2 * x]) - dr), p1 * (__uint_as_float(pr[2 * x + 1]) - dr));
+          }
+          tmem_st16(lane_base + b * 128 + c4 * 16, pk);
         }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(half == 0 ? &sm.ds_a[b] : &sm.ds_b[b]));
       }
     }
     __nv_bfloat16* out = dq + (int64_t)row * ld + (int64_t)h * kD;
@@ -411,33 +425,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        mbar_wait(smem_u32(&sm.sdp_full), it & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
-      const float* l2 = sm.l2[s];
-      const float* dr = sm.dr[s];
+      const float4* l2v = reinterpret_cast<const float4*>(sm.l2[s]);
+      const float4* drv = reinterpret_cast<const float4*>(sm.dr[s]);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t sr[32], pr[32];
-        tmem_ld32(lane_base + c4 * 32, sr);
-        tmem_ld32(lane_base + 128 + c4 * 32, pr);
+      for (int half = 0; half < 2; ++half) {
+        // two 32-column chunks of S^T and dP^T in flight, one wait
+        uint32_t s0[32], s1[32], d0[32], d1[32];
+        tmem_ld32(lane_base + half * 64, s0);
+        tmem_ld32(lane_base + half * 64 + 32, s1);
+        tmem_ld32(lane_base + 128 + half * 64, d0);
+        tmem_ld32(lane_base + 128 + half * 64 + 32, d1);
         tmem_wait_ld();
-        reg_fence(sr);
-        reg_fence(pr);
-        uint32_t pp[16], dd[16];
+        reg_fence(s0);
+        reg_fence(s1);
+        reg_fence(d0);
+        reg_fence(d1);
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int q0 = c4 * 32 + 2 * x;
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * x]), kSl2, -l2[q0]));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * x + 1]), kSl2, -l2[q0 + 1]));
-          pp[x] = pack_bf16x2(p0, p1);
-          dd[x] = pack_bf16x2(p0 * (__uint_as_float(pr[2 * x]) - dr[q0]), p1 * (__uint_as_float(pr[2 * x + 1]) - dr[q0 + 1]));
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c4 = half * 2 + cc;
+          const uint32_t* sr = cc ? s1 : s0;
+          const uint32_t* pr = cc ? d1 : d0;
+          uint32_t pp[16], dd[16];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {  // 4 query columns per vector load of the row statistics
+            const float4 L = l2v[c4 * 8 + q4];
+            const float4 Dv = drv[c4 * 8 + q4];
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4]), kSl2, -L.x));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 1]), kSl2, -L.y));
+            const float p2 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 2]), kSl2, -L.z));
+            const float p3 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 3]), kSl2, -L.w));
+            pp[2 * q4] = pack_bf16x2(p0, p1);
+            pp[2 * q4 + 1] = pack_bf16x2(p2, p3);
+            dd[2 * q4] = pack_bf16x2(p0 * (__uint_as_float(pr[4 * q4]) - Dv.x),
+                                     p1 * (__uint_as_float(pr[4 * q4 + 1]) - Dv.y));
+            dd[2 * q4 + 1] = pack_bf16x2(p2 * (__uint_as_float(pr[4 * q4 + 2]) - Dv.z),
+                                         p3 * (__uint_as_float(pr[4 * q4 + 3]) - Dv.w));
+          }
+          tmem_st16(lane_base + c4 * 16, pp);
+          tmem_st16(lane_base + 128 + c4 * 16, dd);
         }
-        tmem_st16(lane_base + c4 * 16, pp);
-        tmem_st16(lane_base + 128 + c4 * 16, dd);
-        if (c4 == 1 || c4 == 3) {
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(c4 == 1 ? &sm.half_a : &sm.half_b));
-        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(half == 0 ? &sm.half_a : &sm.half_b));
       }
     }
     const int col = j * kB + c;

@@ -245,17 +245,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = block_of(lst, it, nb, jok);
       const int len = jok ? min(kBN, N - j * kBN) : 0;
       if (!jok && r == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
+      // the whole S row: four loads in flight, one wait
       float s[128];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(lane_base + b * 128, r0);
+        tmem_ld32(lane_base + b * 128 + 32, r1);
+        tmem_ld32(lane_base + b * 128 + 64, r2);
+        tmem_ld32(lane_base + b * 128 + 96, r3);
+        tmem_wait_ld();
+        reg_fence(r0);
+        reg_fence(r1);
+        reg_fence(r2);
+        reg_fence(r3);
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t rr[32];
-        tmem_load_row32(lane_base + b * 128 + c4 * 32, rr);
-#pragma unroll
-        for (int x = 0; x < 32; ++x) s[c4 * 32 + x] = __uint_as_float(rr[x]);
+        for (int x = 0; x < 32; ++x) {
+          s[x] = __uint_as_float(r0[x]);
+          s[32 + x] = __uint_as_float(r1[x]);
+          s[64 + x] = __uint_as_float(r2[x]);
+          s[96 + x] = __uint_as_float(r3[x]);
+        }
       }
-      float mx = -INFINITY;
+      if (len < kBN) {  // short or skipped block (warp-uniform): masked keys never count
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx = (c < len) ? fmaxf(mx, s[c]) : mx;
+        for (int c = 0; c < 128; ++c) s[c] = c < len ? s[c] : -INFINITY;
+      }
+      float m8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = s[k];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float m_new = fmaxf(m_used, mx * kSl2);
       if (m_new > m_used + kRescaleLog2) {
         const float alpha = fast_exp2(m_used - m_new);
@@ -275,21 +296,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
         m_used = m_new;
       }
-      const bool live = m_used > -INFINITY;
-      float lsum = 0.f;
+      // no live key yet (only skipped blocks so far): P = 0 (warp-uniform)
+      const float neg_m = m_used > -INFINITY ? -m_used : -INFINITY;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const int c = half * 64 + 2 * x;
-          const float p0 = (live && c < len) ? fast_exp2(fmaf(s[c], kSl2, -m_used)) : 0.f;
-          const float p1 = (live && c + 1 < len) ? fast_exp2(fmaf(s[c + 1], kSl2, -m_used)) : 0.f;
-          lsum += p0 + p1;
+          const float p0 = fast_exp2(fmaf(s[c], kSl2, neg_m));
+          const float p1 = fast_exp2(fmaf(s[c + 1], kSl2, neg_m));
+          ls[x & 3] += p0 + p1;
           pk[x] = pack_bf16x2(p0, p1);
         }
         tmem_st32(lane_base + b * 128 + half * 32, pk);
       }
+      const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tmem_wait_st();
       l += lsum;
       tc_fence_before();
