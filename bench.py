@@ -68,6 +68,24 @@ def job_throughput(work_per_rank: float, world: int, seconds: float) -> float:
     return world * work_per_rank / seconds / 1e12
 
 
+def dram_traffic(workload, kernel):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload`, from the ncu
+    summary table in profiles/traffic.md (rows "| workload | kernel | bytes | ... |"),
+    or None when no capture of the kernel as it stands is recorded."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 3 and cells[0] == workload and cells[1] == kernel:
+                try:
+                    return float(cells[2])
+                except ValueError:
+                    return None
+    return None
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
@@ -212,11 +230,7 @@ def run_ours(args, rank, world, local_rank):
     bound, w = algo.get(dom, ("tensor", 0.0))
     t_launch = per_kernel[dom]["ms_per_launch"] * 1e-3
     w_launch = w / max(1, per_kernel[dom]["launches_per_step"])
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            traffic = json.load(f).get(f"{wl.name}:{dom}")
+    traffic = dram_traffic(wl.name, dom)
     if bound == "tensor":
         achieved = w_launch / t_launch / 1e12
         roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": pk["bf16_sustained"],
