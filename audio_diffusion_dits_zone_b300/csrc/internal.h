@@ -47,7 +47,7 @@ cudaError_t scores_launch(const float* qbar, const float* kbar, int Hh, int nb, 
                           cudaStream_t st);
 
 // select.cu
-cudaError_t select_launch(const float* scores, int Hh, int nb, int k_top, float tau, int32_t* counts,
+cudaError_t select_launch(const float* scores, int Hh, int nb, int k_top, double tau, int32_t* counts,
                           int32_t* idx, cudaStream_t st);
 
 // bsa_simt.cu (CUDA-core attention for f32 inputs and shapes outside the tensor-core path)

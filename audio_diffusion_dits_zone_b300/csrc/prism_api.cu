@@ -201,7 +201,7 @@ int prism_select(const float* scores, int32_t Hh, int32_t nb, double sparsity, d
   if (!(cdf_tau >= 0.0 && cdf_tau <= 1.0)) return fail(PRISM_EINVAL, "cdf_tau must be in [0, 1]");
   const double kk = std::ceil((1.0 - sparsity) * nb - 1e-9);
   const int k_top = (int)std::min<double>(nb, std::max<double>(1.0, kk));
-  cudaError_t e = prism::select_launch(scores, Hh, nb, k_top, (float)cdf_tau, counts, idx,
+  cudaError_t e = prism::select_launch(scores, Hh, nb, k_top, cdf_tau, counts, idx,
                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? (launched(1), ok()) : cuda_fail(e, "prism_select");
 }

@@ -15,12 +15,21 @@
 // clipped at the zone edge, tokens raster inside a tile.
 //
 // Kernels (all HBM-bound or tiny):
-//   zone_partial   one CTA per (zone, channel chunk): the chunk of the zone is
-//                  staged in shared memory (coalesced 16-byte loads) and the
-//                  two-pass line variances are summed for the three axes;
+//   zone_lines     (zones up to 3 x 9 or 5 x 8 in t x h, even channel counts) one warp
+//                  per (zone, 64 channels), lane = 2 channels, so every load is one
+//                  128-byte run of a token row.  The warp streams the zone once,
+//                  w outermost, t innermost, keeping every line sum in registers:
+//                  per channel sum_lines (x - line mean)^2 = sum x^2 - sum_lines
+//                  (line sum)^2 / L, with x taken relative to the zone's first token
+//                  (a shift leaves every line variance unchanged and keeps the two
+//                  terms small);
+//   zone_partial   (any other zone) one CTA per (zone, channel chunk): the chunk is
+//                  staged in shared memory and the two-pass line variances are
+//                  summed for the three axes;
 //   zone_finalize  one CTA per zone: fixed-order sum over chunks, A2V statistics;
 //   zone_choose    one CTA: largest zone mean, per-zone scores, fp32 costs, argmin;
 //   zone_perm      one thread per token: closed-form block-order position.
+#include <algorithm>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -169,6 +178,105 @@ __global__ void __launch_bounds__(kZoneThreads) zone_partial_kernel(const T* __r
   if (threadIdx.x < 3) part[((size_t)z * nchunks + chunk) * 3 + threadIdx.x] = acc[threadIdx.x];
 }
 
+// Two consecutive channels of one token as fp32.
+template <typename T>
+__device__ __forceinline__ float2 load_pair(const T* p);
+template <>
+__device__ __forceinline__ float2 load_pair<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(p));
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float2 load_pair<float>(const float* p) {
+  return __ldg(reinterpret_cast<const float2*>(p));
+}
+
+constexpr int kLinesWarps = 8;
+constexpr int kLinesChannels = 64;  // per warp
+
+// part[(z * nchunks + chunk) * 3 + a] = sum over the chunk's channels and the zone's
+// lines along axis a of sum_x (x - line mean)^2; chunk = 64 channels.
+template <typename T, int MT, int MH>
+__global__ void __launch_bounds__(kLinesWarps * 32) zone_lines_kernel(const T* __restrict__ feat, int64_t ld, int C,
+                                                                      ZoneGeom g, int nchunks,
+                                                                      float* __restrict__ part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kLinesWarps + warp;
+  const int z = blockIdx.y;
+  if (chunk >= nchunks) return;  // warp-uniform; no block-wide synchronisation below
+  const ZoneBox b = zone_box(g, z);
+  const int c = chunk * kLinesChannels + 2 * lane;
+  const bool act = c < C;  // C is even: both channels of the pair exist
+  const int64_t st = (int64_t)g.H * g.W * ld, sh = (int64_t)g.W * ld;
+  const T* zp = feat + (((int64_t)b.t0 * g.H + b.h0) * g.W + b.w0) * ld + (act ? c : 0);
+  const float2 x0 = load_pair<T>(zp);
+  float wsum[MT][MH][2];
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int h = 0; h < MH; ++h) wsum[t][h][0] = wsum[t][h][1] = 0.f;
+  float sq[2] = {0.f, 0.f}, bt[2] = {0.f, 0.f}, bh[2] = {0.f, 0.f};
+  for (int w = 0; w < b.Lw; ++w) {
+    const T* pw = zp + (int64_t)w * ld;
+    float hs[MT][2];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) hs[t][0] = hs[t][1] = 0.f;
+#pragma unroll
+    for (int h = 0; h < MH; ++h) {
+      if (h < b.Lh) {
+        float ts[2] = {0.f, 0.f};
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          if (t < b.Lt) {
+            float2 x = load_pair<T>(pw + h * sh + t * st);
+            x.x -= x0.x;
+            x.y -= x0.y;
+            ts[0] += x.x;
+            ts[1] += x.y;
+            hs[t][0] += x.x;
+            hs[t][1] += x.y;
+            wsum[t][h][0] += x.x;
+            wsum[t][h][1] += x.y;
+            sq[0] = fmaf(x.x, x.x, sq[0]);
+            sq[1] = fmaf(x.y, x.y, sq[1]);
+          }
+        }
+        bt[0] = fmaf(ts[0], ts[0], bt[0]);  // t-line (h, w)
+        bt[1] = fmaf(ts[1], ts[1], bt[1]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {  // h-lines (t, w)
+      bh[0] = fmaf(hs[t][0], hs[t][0], bh[0]);
+      bh[1] = fmaf(hs[t][1], hs[t][1], bh[1]);
+    }
+  }
+  float bw[2] = {0.f, 0.f};
+#pragma unroll
+  for (int t = 0; t < MT; ++t)
+#pragma unroll
+    for (int h = 0; h < MH; ++h) {  // w-lines (t, h); unused slots hold 0
+      bw[0] = fmaf(wsum[t][h][0], wsum[t][h][0], bw[0]);
+      bw[1] = fmaf(wsum[t][h][1], wsum[t][h][1], bw[1]);
+    }
+  float ss[3] = {0.f, 0.f, 0.f};
+  if (act) {
+    const float* bl[3] = {bt, bh, bw};
+    const int L[3] = {b.Lt, b.Lh, b.Lw};
+#pragma unroll
+    for (int a = 0; a < 3; ++a)
+      if (L[a] > 1) {
+        const float inv = 1.f / (float)L[a];
+        ss[a] = fmaxf(sq[0] - bl[a][0] * inv, 0.f) + fmaxf(sq[1] - bl[a][1] * inv, 0.f);
+      }
+  }
+#pragma unroll
+  for (int a = 0; a < 3; ++a)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss[a] += __shfl_xor_sync(0xffffffffu, ss[a], o);
+  if (lane < 3) part[((size_t)z * nchunks + chunk) * 3 + lane] = lane == 0 ? ss[0] : (lane == 1 ? ss[1] : ss[2]);
+}
+
 // stats[z * 8 + {0,1,2}] = v_a, {3,4,5} = u_a, 6 = zone mean of a2v.
 __global__ void __launch_bounds__(kZoneThreads) zone_finalize_kernel(const float* __restrict__ part, int nchunks,
                                                                      const float* __restrict__ a2v, ZoneGeom g,
@@ -293,10 +401,22 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
+// The streaming kernel applies: an instantiated zone size, an even channel count and
+// row stride, and channel pairs aligned for one 4-byte (bf16) or 8-byte (f32) load.
+int lines_variant(const ZoneGeom& g, int C, int64_t ld, int dtype, const void* feat) {
+  const size_t al = dtype == PRISM_BF16 ? 4 : 8;
+  if (C % 2 != 0 || ld % 2 != 0 || (reinterpret_cast<uintptr_t>(feat) % al) != 0) return 0;
+  const int Lt = std::min(g.zt, g.T), Lh = std::min(g.zh, g.H);
+  if (Lt <= 3 && Lh <= 9) return 1;
+  if (Lt <= 5 && Lh <= 8) return 2;
+  return 0;
+}
+
 size_t zone_ws_bytes(const ZoneGeom& g, int C, int /*dtype*/) {
+  // both kernels write partials per 64-channel chunk (zone_partial: chunk <= 64)
   const int ch = chunk_channels(g);
   if (ch == 0) return 0;
-  const int nchunks = (C + ch - 1) / ch;
+  const int nchunks = std::max((C + ch - 1) / ch, (C + kLinesChannels - 1) / kLinesChannels);
   return align256((size_t)g.Z * nchunks * 3 * sizeof(float)) + align256((size_t)g.Z * 8 * sizeof(float));
 }
 
@@ -304,13 +424,33 @@ cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const fl
                         const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm, void* ws, cudaStream_t st,
                         uint32_t* /*status*/) {
   const int ch = chunk_channels(g);
-  const int nchunks = (C + ch - 1) / ch;
+  const int variant = lines_variant(g, C, ld, dtype, feat);
+  const int nchunks = variant ? (C + kLinesChannels - 1) / kLinesChannels : (C + ch - 1) / ch;
+  const int ws_chunks = std::max((C + ch - 1) / ch, (C + kLinesChannels - 1) / kLinesChannels);
   float* part = reinterpret_cast<float*>(ws);
-  float* stats = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)g.Z * nchunks * 3 * 4));
+  float* stats = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)g.Z * ws_chunks * 3 * 4));
   const size_t smem = (size_t)g.max_tokens * ch * sizeof(float);
   const dim3 grid(g.Z, nchunks);
   cudaError_t e;
-  if (dtype == PRISM_BF16) {
+  if (variant) {
+    const dim3 lgrid((nchunks + kLinesWarps - 1) / kLinesWarps, g.Z);
+    HookScope hs("zone_lines", st);
+    if (dtype == PRISM_BF16) {
+      if (variant == 1)
+        zone_lines_kernel<__nv_bfloat16, 3, 9><<<lgrid, kLinesWarps * 32, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(feat), ld, C, g, nchunks, part);
+      else
+        zone_lines_kernel<__nv_bfloat16, 5, 8><<<lgrid, kLinesWarps * 32, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(feat), ld, C, g, nchunks, part);
+    } else {
+      if (variant == 1)
+        zone_lines_kernel<float, 3, 9><<<lgrid, kLinesWarps * 32, 0, st>>>(static_cast<const float*>(feat), ld, C, g,
+                                                                            nchunks, part);
+      else
+        zone_lines_kernel<float, 5, 8><<<lgrid, kLinesWarps * 32, 0, st>>>(static_cast<const float*>(feat), ld, C, g,
+                                                                            nchunks, part);
+    }
+  } else if (dtype == PRISM_BF16) {
     const bool vec = (ld % 8 == 0) && (C % 8 == 0) && ((reinterpret_cast<uintptr_t>(feat) & 15) == 0);
     if (vec) {
       auto k = zone_partial_kernel<__nv_bfloat16, 8>;
