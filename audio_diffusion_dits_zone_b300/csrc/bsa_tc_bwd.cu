@@ -47,27 +47,33 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) {  // MN-major
 }
 
 // ------------------------------------------------------------------- prep
-__global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-                                const float* __restrict__ lse, int64_t ld, int N, int Hh, int npad,
-                                float* __restrict__ L2, float* __restrict__ Dp) {
-  // one warp per (head, padded row)
-  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= (int64_t)Hh * npad) return;
-  const int h = (int)(wid / npad), r = (int)(wid - (int64_t)h * npad);
+// 16 threads per (head, padded row), 8 channels (one 16-byte load of O and of dO) each.
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dO,
+                                                       const float* __restrict__ lse, int64_t ld, int N, int Hh,
+                                                       int npad, float* __restrict__ L2, float* __restrict__ Dp) {
+  const int64_t gid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+  const int sub = threadIdx.x & 15;
+  if (gid >= (int64_t)Hh * npad) return;  // 16-lane groups are whole: the group exits together
+  // rows fastest within a head, so consecutive groups read consecutive token rows
+  const int h = (int)(gid / npad), r = (int)(gid - (int64_t)h * npad);
   float s = 0.f;
   if (r < N) {
-    const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(o + (int64_t)r * ld + (int64_t)h * kD);
-    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(dO + (int64_t)r * ld + (int64_t)h * kD);
+    const int64_t off = (int64_t)r * ld + (int64_t)h * kD + sub * 8;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + off));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + off));
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-    for (int c = lane; c < kD / 2; c += 32) {
-      const float2 x = __bfloat1622float2(a[c]), y = __bfloat1622float2(b[c]);
+    for (int k = 0; k < 4; ++k) {
+      const float2 x = __bfloat1622float2(a2[k]), y = __bfloat1622float2(b2[k]);
       s = fmaf(x.x, y.x, fmaf(x.y, y.y, s));
     }
   }
+  const unsigned grp = 0xffffu << (threadIdx.x & 16);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) {
+  for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(grp, s, off);
+  if (sub == 0) {
     const size_t at = (size_t)h * npad + r;
     Dp[at] = r < N ? s : 0.f;
     L2[at] = r < N ? lse[(size_t)h * N + r] * kLog2e : INFINITY;
@@ -524,7 +530,7 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
   const int npad = nb * kB;
   float* L2 = rowstats;
   float* Dp = rowstats + (size_t)Hh * npad;
-  const int64_t threads = (int64_t)Hh * npad * 32;
+  const int64_t threads = (int64_t)Hh * npad * 16;
   {
     HookScope hs("bwd_prep", st);
     bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(

@@ -63,6 +63,32 @@ bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_
   return r == CUDA_SUCCESS;
 }
 
+bool tensor_map_bf16(void* map_out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                     const uint32_t* box) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int k = 0; k < rank; ++k) {
+    d[k] = dims[k];
+    bx[k] = box[k];
+    es[k] = 1;
+    if (k + 1 < rank) st[k] = strides_bytes[k];
+  }
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                              const_cast<void*>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 constexpr int kBM = 128;   // query rows per tile
@@ -323,7 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = i * kBM + r;
     __nv_bfloat16* orow = o + (int64_t)row * ld + (int64_t)h * kD;
     if (ok && cnt > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_bar), (cnt - 1) & 1, abort, status));
+      // every MMA of the CTA has completed once mma_done flips; it completes once, so its
+      // parity cannot alias an older phase (o_bar may still be two phases behind here)
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.mma_done), 0, abort, status));
       if (ok) {
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;

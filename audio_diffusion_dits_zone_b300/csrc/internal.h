@@ -80,5 +80,9 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                         uint32_t box_inner, uint32_t box_outer);
+// bf16 tensor map of rank 1..5, no swizzle: dims innermost first, strides_bytes[k] =
+// byte stride of dimension k + 1.
+bool tensor_map_bf16(void* map_out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                     const uint32_t* box);
 
 }  // namespace prism

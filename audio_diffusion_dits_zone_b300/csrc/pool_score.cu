@@ -131,49 +131,107 @@ __global__ void __launch_bounds__(kPoolThreads)
   }
 }
 
-constexpr int kTile = 64, kKc = 32;
+// scores: S = qbar kbar^T / sqrt(d) per head, fp32 on CUDA cores.  A CTA of 256
+// threads owns a 128 x 128 tile of S; each thread an 8 x 8 register tile (rows
+// ty + 16u, columns tx + 16w).  k-slices of 16 are staged in shared memory,
+// transposed (k-major), double-buffered through registers so the next slice's
+// global loads overlap this slice's 8 x 8 x 16 FMAs.
+constexpr int kSTile = 128, kSK = 16, kSThreads = 256;
 
-__global__ void __launch_bounds__(256) scores_kernel(const float* __restrict__ qbar, const float* __restrict__ kbar,
-                                                     int nb, int d, float scale, float* __restrict__ S) {
-  __shared__ float As[kKc][kTile + 4];
-  __shared__ float Bs[kKc][kTile + 4];
+__global__ void __launch_bounds__(kSThreads) scores_kernel(const float* __restrict__ qbar,
+                                                           const float* __restrict__ kbar, int nb, int d,
+                                                           float scale, float* __restrict__ S) {
+  __shared__ __align__(16) float As[2][kSK][kSTile + 4];
+  __shared__ __align__(16) float Bs[2][kSK][kSTile + 4];
   const int h = blockIdx.z;
-  const int i0 = blockIdx.y * kTile, j0 = blockIdx.x * kTile;
+  const int i0 = blockIdx.y * kSTile, j0 = blockIdx.x * kSTile;
   const float* A = qbar + (size_t)h * nb * d;
   const float* Bm = kbar + (size_t)h * nb * d;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4] = {};
-  for (int c0 = 0; c0 < d; c0 += kKc) {
-    for (int e = threadIdx.x; e < kTile * kKc; e += 256) {
-      const int r = e / kKc, c = e - (e / kKc) * kKc;
-      const bool okc = c0 + c < d;
-      As[c][r] = (i0 + r < nb && okc) ? A[(size_t)(i0 + r) * d + c0 + c] : 0.f;
-      Bs[c][r] = (j0 + r < nb && okc) ? Bm[(size_t)(j0 + r) * d + c0 + c] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int c = 0; c < kKc; ++c) {
-      float a[4], bb[4];
+  // loader: each thread brings 8 values of A and 8 of B per k-slice: rows lr, lr + 64;
+  // columns lc .. lc + 3 (one float4 when d allows it)
+  const int lr = threadIdx.x >> 2, lc = (threadIdx.x & 3) * 4;
+  const bool vec = (d & 3) == 0;
+  float4 ra[2], rb[2];
+  auto load = [&](int k0) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        a[u] = As[c][ty + 16 * u];
-        bb[u] = Bs[c][tx + 16 * u];
+    for (int u = 0; u < 2; ++u) {
+      const int ri = i0 + lr + 64 * u, rj = j0 + lr + 64 * u;
+      float a[4], b[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] = b[e] = 0.f;
+      if (vec && k0 + lc + 3 < d) {
+        if (ri < nb) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(A + (size_t)ri * d + k0 + lc));
+          a[0] = x.x, a[1] = x.y, a[2] = x.z, a[3] = x.w;
+        }
+        if (rj < nb) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(Bm + (size_t)rj * d + k0 + lc));
+          b[0] = x.x, b[1] = x.y, b[2] = x.z, b[3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = k0 + lc + e;
+          if (c < d && ri < nb) a[e] = A[(size_t)ri * d + c];
+          if (c < d && rj < nb) b[e] = Bm[(size_t)rj * d + c];
+        }
+      }
+      ra[u] = make_float4(a[0], a[1], a[2], a[3]);
+      rb[u] = make_float4(b[0], b[1], b[2], b[3]);
+    }
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int r = lr + 64 * u;
+      As[buf][lc][r] = ra[u].x;
+      As[buf][lc + 1][r] = ra[u].y;
+      As[buf][lc + 2][r] = ra[u].z;
+      As[buf][lc + 3][r] = ra[u].w;
+      Bs[buf][lc][r] = rb[u].x;
+      Bs[buf][lc + 1][r] = rb[u].y;
+      Bs[buf][lc + 2][r] = rb[u].z;
+      Bs[buf][lc + 3][r] = rb[u].w;
+    }
+  };
+  float acc[8][8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+#pragma unroll
+    for (int w = 0; w < 8; ++w) acc[u][w] = 0.f;
+  const int nk = (d + kSK - 1) / kSK;
+  load(0);
+  store(0);
+  __syncthreads();
+  for (int kt = 0; kt < nk; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < nk) load((kt + 1) * kSK);
+#pragma unroll
+    for (int c = 0; c < kSK; ++c) {
+      float a[8], b[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        a[u] = As[buf][c][ty + 16 * u];
+        b[u] = Bs[buf][c][tx + 16 * u];
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 8; ++u)
 #pragma unroll
-        for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(a[u], bb[w], acc[u][w]);
+        for (int w = 0; w < 8; ++w) acc[u][w] = fmaf(a[u], b[w], acc[u][w]);
     }
+    if (kt + 1 < nk) store(buf ^ 1);
     __syncthreads();
   }
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
+  for (int u = 0; u < 8; ++u) {
     const int i = i0 + ty + 16 * u;
     if (i >= nb) continue;
+    float* row = S + ((size_t)h * nb + i) * nb;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < 8; ++w) {
       const int j = j0 + tx + 16 * w;
-      if (j < nb) S[((size_t)h * nb + i) * nb + j] = acc[u][w] * scale;
+      if (j < nb) row[j] = acc[u][w] * scale;
     }
   }
 }
@@ -211,9 +269,9 @@ cudaError_t pool_launch(const void* q, const void* k, const void* v, int dtype, 
 
 cudaError_t scores_launch(const float* qbar, const float* kbar, int Hh, int nb, int d, float* scores,
                           cudaStream_t st) {
-  const dim3 grid((nb + kTile - 1) / kTile, (nb + kTile - 1) / kTile, Hh);
+  const dim3 grid((nb + kSTile - 1) / kSTile, (nb + kSTile - 1) / kSTile, Hh);
   HookScope hs("scores", st);
-  scores_kernel<<<grid, 256, 0, st>>>(qbar, kbar, nb, d, 1.0f / sqrtf((float)d), scores);
+  scores_kernel<<<grid, kSThreads, 0, st>>>(qbar, kbar, nb, d, 1.0f / sqrtf((float)d), scores);
   return cudaGetLastError();
 }
 

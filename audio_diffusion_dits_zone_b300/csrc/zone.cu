@@ -15,6 +15,12 @@
 // clipped at the zone edge, tokens raster inside a tile.
 //
 // Kernels (all HBM-bound or tiny):
+//   zone_tma       (bf16 features, zones up to 3 x 9 x 16) persistent CTAs of 4 warps;
+//                  each warp streams its own (zone, 64-channel) items as two 32-channel
+//                  slabs: one 4D TMA box [t][h][w][32 channels] per slab into a
+//                  double-buffered shared-memory stage, so the next slab is in flight
+//                  while this one is reduced (lane = channel, all line sums in
+//                  registers, same arithmetic as zone_lines);
 //   zone_lines     (zones up to 3 x 9 or 5 x 8 in t x h, even channel counts) one warp
 //                  per (zone, 64 channels), lane = 2 channels, so every load is one
 //                  128-byte run of a token row.  The warp streams the zone once,
@@ -30,6 +36,7 @@
 //   zone_choose    one CTA: largest zone mean, per-zone scores, fp32 costs, argmin;
 //   zone_perm      one thread per token: closed-form block-order position.
 #include <algorithm>
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -277,6 +284,118 @@ __global__ void __launch_bounds__(kLinesWarps * 32) zone_lines_kernel(const T* _
   if (lane < 3) part[((size_t)z * nchunks + chunk) * 3 + lane] = lane == 0 ? ss[0] : (lane == 1 ? ss[1] : ss[2]);
 }
 
+constexpr int kTmaWarps = 4;
+constexpr int kSlabCh = 32;                        // channels per slab (64 bytes per token)
+constexpr int kSlabMaxBytes = 3 * 9 * 16 * kSlabCh * 2;  // one 3 x 9 x 16 zone box
+constexpr int kTmaStages = 2;                      // per warp
+
+struct ZoneTmaSmem {
+  uint8_t slab[kTmaWarps][kTmaStages][kSlabMaxBytes];
+  uint64_t full[kTmaWarps][kTmaStages];
+};
+
+// part[(z * nchunks + chunk) * 3 + a] exactly as zone_lines_kernel (chunk = 64 channels),
+// from slabs loaded with the 4D tensor map tm = feature viewed as [T][H][W][C] bf16.
+template <int MT, int MH>
+__global__ void __launch_bounds__(kTmaWarps * 32, 1)
+    zone_tma_kernel(const __grid_constant__ CUtensorMap tm, ZoneGeom g, int nchunks, int items,
+                    float* __restrict__ part, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  ZoneTmaSmem& sm = *reinterpret_cast<ZoneTmaSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slab_bytes = g.zt * g.zh * g.zw * kSlabCh * 2;
+  if (lane == 0) {
+    for (int s = 0; s < kTmaStages; ++s) mbar_init(smem_u32(&sm.full[warp][s]), 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  // this warp's items: k = (blockIdx.x * kTmaWarps + warp) + n * stride, two slabs each
+  const int stride = gridDim.x * kTmaWarps;
+  const int first = blockIdx.x * kTmaWarps + warp;
+  const int nmine = first < items ? (items - first + stride - 1) / stride : 0;
+  const int nslabs = 2 * nmine;
+  auto issue = [&](int s) {  // slab s of this warp -> stage s & 1
+    const int k = first + (s >> 1) * stride;
+    const int z = k / nchunks, chunk = k - z * nchunks;
+    const ZoneBox b = zone_box(g, z);
+    const uint32_t bar = smem_u32(&sm.full[warp][s & 1]);
+    mbar_arrive_expect_tx(bar, (uint32_t)slab_bytes);
+    tma_load_4d(smem_u32(sm.slab[warp][s & 1]), &tm, chunk * 64 + (s & 1) * kSlabCh, b.w0, b.h0, b.t0, bar);
+  };
+  int issued = 0;  // lane 0: slabs issued so far
+  if (lane == 0) {
+    tma_prefetch_desc(&tm);
+    for (int s = 0; s < kTmaStages && s < nslabs; ++s) issue(s), ++issued;
+  }
+  int abort = 0;
+  float ss[3] = {0.f, 0.f, 0.f};
+  for (int s = 0; s < nslabs; ++s) {
+    const int k = first + (s >> 1) * stride;
+    const int z = k / nchunks, chunk = k - z * nchunks;
+    const ZoneBox b = zone_box(g, z);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[warp][s & 1]), (s >> 1) & 1, &abort, status));
+    if (!ok) break;
+    // slab layout [t][h][w][32 channels] bf16 with the full box extents (zt, zh, zw);
+    // positions past a clipped zone's edge hold zeros and are skipped
+    const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(sm.slab[warp][s & 1]) + lane;
+    const int sw = kSlabCh, shh = g.zw * kSlabCh, stt = g.zh * g.zw * kSlabCh;
+    const float x0 = __bfloat162float(xs[0]);
+    float wsum[MT][MH];
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int h = 0; h < MH; ++h) wsum[t][h] = 0.f;
+    float sq = 0.f, bt = 0.f, bh = 0.f;
+    for (int w = 0; w < b.Lw; ++w) {
+      float hs[MT];
+#pragma unroll
+      for (int t = 0; t < MT; ++t) hs[t] = 0.f;
+#pragma unroll
+      for (int h = 0; h < MH; ++h) {
+        float ts = 0.f;
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          const bool in = h < b.Lh && t < b.Lt;
+          const float v = in ? __bfloat162float(xs[t * stt + h * shh + w * sw]) - x0 : 0.f;
+          ts += v;
+          hs[t] += v;
+          wsum[t][h] += v;
+          sq = fmaf(v, v, sq);
+        }
+        bt = fmaf(ts, ts, bt);
+      }
+#pragma unroll
+      for (int t = 0; t < MT; ++t) bh = fmaf(hs[t], hs[t], bh);
+    }
+    // every lane has read the stage: refill it with slab s + 2
+    __syncwarp();
+    if (lane == 0 && s + kTmaStages < nslabs) issue(s + kTmaStages), ++issued;
+    float bw = 0.f;
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+#pragma unroll
+      for (int h = 0; h < MH; ++h) bw = fmaf(wsum[t][h], wsum[t][h], bw);
+    const float bl[3] = {bt, bh, bw};
+    const int L[3] = {b.Lt, b.Lh, b.Lw};
+#pragma unroll
+    for (int a = 0; a < 3; ++a)
+      if (L[a] > 1) ss[a] += fmaxf(sq - bl[a] / (float)L[a], 0.f);
+    if (s & 1) {  // both halves of the item done: one partial per (zone, 64 channels)
+#pragma unroll
+      for (int a = 0; a < 3; ++a)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss[a] += __shfl_xor_sync(0xffffffffu, ss[a], o);
+      if (lane < 3) part[((size_t)z * nchunks + chunk) * 3 + lane] = lane == 0 ? ss[0] : (lane == 1 ? ss[1] : ss[2]);
+      ss[0] = ss[1] = ss[2] = 0.f;
+    }
+  }
+  // a warp that gave up waits (bounded) for the copies it still has in flight: the
+  // last slab issued into each stage completes that stage's phase (slab >> 1) & 1
+  if (abort && lane == 0)
+    for (int s = issued - 1; s >= 0 && s >= issued - kTmaStages; --s)
+      drain_wait(smem_u32(&sm.full[warp][s & 1]), (s >> 1) & 1);
+}
+
 // stats[z * 8 + {0,1,2}] = v_a, {3,4,5} = u_a, 6 = zone mean of a2v.
 __global__ void __launch_bounds__(kZoneThreads) zone_finalize_kernel(const float* __restrict__ part, int nchunks,
                                                                      const float* __restrict__ a2v, ZoneGeom g,
@@ -403,6 +522,13 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // The streaming kernel applies: an instantiated zone size, an even channel count and
 // row stride, and channel pairs aligned for one 4-byte (bf16) or 8-byte (f32) load.
+// The TMA kernel applies: bf16, 16-byte aligned rows (ld % 8 == 0), whole 64-channel
+// chunks, zones of at most 3 x 9 x 16 tokens.
+bool tma_variant(const ZoneGeom& g, int C, int64_t ld, int dtype, const void* feat) {
+  return dtype == PRISM_BF16 && C % 64 == 0 && ld % 8 == 0 && (reinterpret_cast<uintptr_t>(feat) & 15) == 0 &&
+         std::min(g.zt, g.T) <= 3 && std::min(g.zh, g.H) <= 9 && std::min(g.zw, g.W) <= 16;
+}
+
 int lines_variant(const ZoneGeom& g, int C, int64_t ld, int dtype, const void* feat) {
   const size_t al = dtype == PRISM_BF16 ? 4 : 8;
   if (C % 2 != 0 || ld % 2 != 0 || (reinterpret_cast<uintptr_t>(feat) % al) != 0) return 0;
@@ -422,17 +548,41 @@ size_t zone_ws_bytes(const ZoneGeom& g, int C, int /*dtype*/) {
 
 cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const float* a2v, const ZoneGeom& g,
                         const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm, void* ws, cudaStream_t st,
-                        uint32_t* /*status*/) {
+                        uint32_t* status) {
   const int ch = chunk_channels(g);
   const int variant = lines_variant(g, C, ld, dtype, feat);
-  const int nchunks = variant ? (C + kLinesChannels - 1) / kLinesChannels : (C + ch - 1) / ch;
+  const bool by64 = variant || tma_variant(g, C, ld, dtype, feat);
+  const int nchunks = by64 ? (C + kLinesChannels - 1) / kLinesChannels : (C + ch - 1) / ch;
   const int ws_chunks = std::max((C + ch - 1) / ch, (C + kLinesChannels - 1) / kLinesChannels);
   float* part = reinterpret_cast<float*>(ws);
   float* stats = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)g.Z * ws_chunks * 3 * 4));
   const size_t smem = (size_t)g.max_tokens * ch * sizeof(float);
   const dim3 grid(g.Z, nchunks);
   cudaError_t e;
-  if (variant) {
+  if (tma_variant(g, C, ld, dtype, feat)) {
+    // feature as [T][H][W][C] bf16; the box is one zone (clipped zones read zeros past the grid)
+    CUtensorMap tm;
+    const uint64_t dims[4] = {(uint64_t)C, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.T};
+    const uint64_t strides[3] = {(uint64_t)ld * 2, (uint64_t)g.W * ld * 2, (uint64_t)g.H * g.W * ld * 2};
+    const uint32_t box[4] = {(uint32_t)kSlabCh, (uint32_t)std::min(g.zw, g.W), (uint32_t)std::min(g.zh, g.H),
+                             (uint32_t)std::min(g.zt, g.T)};
+    ZoneGeom gb = g;  // slab layout uses the box extents
+    gb.zt = (int)box[3], gb.zh = (int)box[2], gb.zw = (int)box[1];
+    if (!tensor_map_bf16(&tm, feat, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    const int items = g.Z * nchunks;
+    int sms = 148;
+    {
+      int dev = 0;
+      if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int grid = std::max(1, std::min(sms, (items + kTmaWarps - 1) / kTmaWarps));
+    const size_t smem_t = sizeof(ZoneTmaSmem) + 128;
+    if ((e = cudaFuncSetAttribute(zone_tma_kernel<3, 9>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t)) !=
+        cudaSuccess)
+      return e;
+    HookScope hs("zone_tma", st);
+    zone_tma_kernel<3, 9><<<grid, kTmaWarps * 32, smem_t, st>>>(tm, gb, nchunks, items, part, status);
+  } else if (variant) {
     const dim3 lgrid((nchunks + kLinesWarps - 1) / kLinesWarps, g.Z);
     HookScope hs("zone_lines", st);
     if (dtype == PRISM_BF16) {
