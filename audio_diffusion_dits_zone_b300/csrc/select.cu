@@ -11,26 +11,28 @@
 // the kept set is the shortest prefix that holds at least k blocks AND at least
 // tau of the mass; emit it in ascending index order.
 //
-// One CTA of 128 threads per (head, query block); no sort.  The row is read once
-// into shared memory as order-preserving 32-bit keys.  The end of the kept prefix
-// is found by a radix descent over the key bits (4 digits of 8 bits, most
-// significant first): at each digit a 256-bin histogram of the candidates' counts
-// and softmax masses picks the first bin, from the top, at which both conditions
-// hold, and the descent continues inside it.  After the last digit the cut is one
-// exact score value; equal scores there are taken in index order.
-//
+// One warp per (head, query block); no sort and no block-wide barrier.  The warp
+// reads its row once into shared memory, then:
+//   1. drops every block into one of 256 equal-width buckets of [min, max] score
+//      (a monotone map), with a histogram of counts and softmax masses;
+//   2. scans the buckets from the top to the first one at which both conditions
+//      hold: everything above it is kept, nothing below it;
+//   3. ranks that bucket's blocks exactly (score descending, index ascending) and
+//      keeps the shortest prefix of them that completes both conditions;
+//   4. writes the kept indices in ascending order with ballots.
 // Masses are fixed-point integers, q = round(exp(s - max) * 2^40), so every sum is
-// exact and independent of the order the threads add in: the lists are
+// exact and independent of the order the lanes add in: the lists are
 // deterministic, and the sums are closer to the exact softmax mass than an fp32
 // running sum would be (the only rounding is in exp and in q, <= 2^-41 per block).
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace prism {
 namespace {
 
-constexpr int kSelThreads = 128;
-constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelWarpsMax = 4;
 constexpr int kBins = 256;
 constexpr float kMassScale = 1099511627776.0f;  // 2^40
 
@@ -39,249 +41,229 @@ __device__ __forceinline__ uint32_t order_bits(float f) {
   if (u == 0x80000000u) u = 0u;  // -0 and +0 are the same score
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // ascending uint order == ascending float order
 }
-__device__ __forceinline__ float from_order_bits(uint32_t o) {
-  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+__device__ __forceinline__ unsigned long long mass_of(float s, float smax) {
+  return __float2ull_rn(expf(s - smax) * kMassScale);
 }
-__device__ __forceinline__ unsigned long long mass_of(uint32_t key, float smax) {
-  return __float2ull_rn(expf(from_order_bits(key) - smax) * kMassScale);
+__device__ __forceinline__ int bucket_of(float s, float smin, float scale) {
+  return min(kBins - 1, max(0, __float2int_rz((s - smin) * scale)));
 }
 
-struct SelShared {
+struct WarpBins {
   uint32_t cnt[kBins];
   unsigned long long mass[kBins];
-  float fmax[kSelWarps];
-  unsigned long long usum[kSelWarps];
-  uint32_t scan[kSelWarps];
-  // descent state, written by warp 0
-  uint32_t prefix, above_cnt, pick_cnt;
-  unsigned long long above_mass;
-  int done;
 };
 
-// Inclusive scan of v over the block; every thread gets its inclusive prefix and
-// the block total.
-__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t* tmp, uint32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) tmp[warp] = x;
-  __syncthreads();
-  uint32_t before = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) {
-    const uint32_t t = tmp[w];
-    before += w < warp ? t : 0u;
-    tot += t;
-  }
-  *total = tot;
-  __syncthreads();
-  return before + x;
+// Per-warp shared memory: the row's scores, a kept flag per block, the crossing
+// bucket's block indices (in index order), then the histogram.
+__host__ __device__ constexpr size_t warp_bytes(int nb) {
+  return ((size_t)nb * (4 + 1 + 4) + 15) / 16 * 16 + sizeof(WarpBins);
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const float* __restrict__ scores, int nb, int k_top,
-                                                             double tau, int32_t* __restrict__ counts,
-                                                             int32_t* __restrict__ idx) {
-  extern __shared__ uint32_t keys[];  // [nb]
-  __shared__ SelShared sh;
+__global__ void __launch_bounds__(kSelWarpsMax * 32) select_kernel(const float* __restrict__ scores, int rows,
+                                                                    int nb, int k_top, double tau,
+                                                                    int32_t* __restrict__ counts,
+                                                                    int32_t* __restrict__ idx) {
+  extern __shared__ __align__(16) uint8_t smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const size_t row = blockIdx.x;
-  const float* s = scores + row * nb;
+  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (row >= rows) return;  // whole warp; nothing below synchronises across warps
+  uint8_t* base = smem + warp * warp_bytes(nb);
+  float* sv = reinterpret_cast<float*>(base);
+  int32_t* cand = reinterpret_cast<int32_t*>(base + (size_t)nb * 4);
+  uint8_t* kept = base + (size_t)nb * 8;
+  WarpBins& B = *reinterpret_cast<WarpBins*>(base + ((size_t)nb * 9 + 15) / 16 * 16);
+  const float* s = scores + (size_t)row * nb;
 
-  // ---- read the row once: keys and the row max
-  float mx = -INFINITY;
-  for (int t = threadIdx.x; t < nb; t += kSelThreads) {
+  // ---- 1. read the row; min and max
+  float mx = -INFINITY, mn = INFINITY;
+  for (int t = lane; t < nb; t += 32) {
     const float v = s[t];
-    keys[t] = order_bits(v);
+    sv[t] = v;
+    kept[t] = 0;
     mx = fmaxf(mx, v);
+    mn = fminf(mn, v);
+  }
+  for (int b = lane; b < kBins; b += 32) {
+    B.cnt[b] = 0u;
+    B.mass[b] = 0ull;
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) sh.fmax[warp] = mx;
-  __syncthreads();
-  float smax = sh.fmax[0];
-#pragma unroll
-  for (int w = 1; w < kSelWarps; ++w) smax = fmaxf(smax, sh.fmax[w]);
-
-  // ---- total mass (integer, exact)
-  unsigned long long z = 0;
-  for (int t = threadIdx.x; t < nb; t += kSelThreads) z += mass_of(keys[t], smax);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  if (lane == 0) sh.usum[warp] = z;
-  if (threadIdx.x == 0) {
-    sh.prefix = 0u;
-    sh.above_cnt = 0u;
-    sh.above_mass = 0ull;
-    sh.done = 0;
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
   }
-  __syncthreads();
-  unsigned long long ztot = 0;
-#pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) ztot += sh.usum[w];
-  const double target = tau * (double)ztot;
-  const uint32_t kneed = (uint32_t)k_top;
-
-  // ---- radix descent: 4 digits of 8 bits
-  uint32_t mask = 0u;
-  for (int level = 0; level < 4; ++level) {
-    const int shift = 24 - 8 * level;
-    for (int b = threadIdx.x; b < kBins; b += kSelThreads) {
-      sh.cnt[b] = 0u;
-      sh.mass[b] = 0ull;
-    }
-    __syncthreads();
-    const uint32_t prefix = sh.prefix;
-    // warp-aggregated histogram: lanes that hit the same bin add once
-    for (int t0 = 0; t0 < nb; t0 += kSelThreads) {
-      const int t = t0 + threadIdx.x;
-      uint32_t key = 0u;
-      bool cand = false;
-      if (t < nb) {
-        key = keys[t];
-        cand = (key & mask) == prefix;
-      }
-      const uint32_t act = __ballot_sync(0xffffffffu, cand);
-      if (!act) continue;
-      const uint32_t bin = cand ? (key >> shift) & 0xffu : 0x100u + lane;  // non-candidates never match a bin
-      const uint32_t grp = __match_any_sync(0xffffffffu, bin);
-      const unsigned long long q = cand ? mass_of(key, smax) : 0ull;
-      const uint32_t qhi = (uint32_t)(q >> 20), qlo = (uint32_t)(q & 0xfffffu);  // q <= 2^40
-      const uint32_t shi = __reduce_add_sync(grp, qhi), slo = __reduce_add_sync(grp, qlo);
-      if (cand && lane == __ffs(grp) - 1) {
-        atomicAdd(&sh.cnt[bin], (uint32_t)__popc(grp));
-        atomicAdd(&sh.mass[bin], ((unsigned long long)shi << 20) + (unsigned long long)slo);
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins 255 - 8l ... 248 - 8l (descending score order)
-      uint32_t c8[8];
-      unsigned long long m8[8];
-      uint32_t cl = 0u;
-      unsigned long long ml = 0ull;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int b = kBins - 1 - 8 * lane - e;
-        c8[e] = sh.cnt[b];
-        m8[e] = sh.mass[b];
-        cl += c8[e];
-        ml += m8[e];
-      }
-      uint32_t ci = cl;
-      unsigned long long mi = ml;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t cy = __shfl_up_sync(0xffffffffu, ci, o);
-        const unsigned long long my = __shfl_up_sync(0xffffffffu, mi, o);
-        if (lane >= o) {
-          ci += cy;
-          mi += my;
-        }
-      }
-      uint32_t c_run = sh.above_cnt + (ci - cl);
-      unsigned long long m_run = sh.above_mass + (mi - ml);
-      // first bin (from the top) at which both conditions hold; also the lane's last
-      // non-empty bin, the fallback should no bin qualify (only with NaN scores)
-      int hit = -1, last = -1;
-      uint32_t hit_cb = 0u, hit_c = 0u, last_cb = 0u, last_c = 0u;
-      unsigned long long hit_mb = 0ull, last_mb = 0ull;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (c8[e] > 0u) {
-          if (hit < 0 && c_run + c8[e] >= kneed && (double)(m_run + m8[e]) >= target) {
-            hit = e;
-            hit_cb = c_run;
-            hit_mb = m_run;
-            hit_c = c8[e];
-          }
-          last = e;
-          last_cb = c_run;
-          last_mb = m_run;
-          last_c = c8[e];
-        }
-        c_run += c8[e];
-        m_run += m8[e];
-      }
-      const uint32_t hits = __ballot_sync(0xffffffffu, hit >= 0);
-      const uint32_t nonempty = __ballot_sync(0xffffffffu, last >= 0);
-      const int src = hits ? __ffs(hits) - 1 : (nonempty ? 31 - __clz(nonempty) : -1);
-      if (lane == src) {
-        const bool h = hits != 0u;
-        const uint32_t b = (uint32_t)(kBins - 1 - 8 * lane - (h ? hit : last));
-        sh.prefix = prefix | (b << shift);
-        sh.above_cnt = h ? hit_cb : last_cb;
-        sh.above_mass = h ? hit_mb : last_mb;
-        sh.pick_cnt = h ? hit_c : last_c;
-      }
-    }
-    mask |= 0xffu << shift;
-    __syncthreads();
+  const float range = mx - mn;
+  const float scale = range > 0.f ? (float)kBins / range : 0.f;
+  __syncwarp();
+  // ---- histogram of counts and masses
+  for (int t = lane; t < nb; t += 32) {
+    const float v = sv[t];
+    const int b = bucket_of(v, mn, scale);
+    atomicAdd(&B.cnt[b], 1u);
+    atomicAdd(&B.mass[b], mass_of(v, mx));
   }
-
-  // ---- the cut: keys above V are kept; of the keys equal to V (one score value,
-  // equal masses), the first `take` in index order
-  const uint32_t V = sh.prefix;
-  const uint32_t above = sh.above_cnt, neq = sh.pick_cnt;
-  const unsigned long long above_m = sh.above_mass;
-  uint32_t take;
+  __syncwarp();
+  // ---- 2. scan from the top bucket; lane l owns buckets 255 - 8l ... 248 - 8l
+  uint32_t c8[8];
+  unsigned long long m8[8];
+  uint32_t cl = 0u;
+  unsigned long long ml = 0ull;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int b = kBins - 1 - 8 * lane - e;
+    c8[e] = B.cnt[b];
+    m8[e] = B.mass[b];
+    cl += c8[e];
+    ml += m8[e];
+  }
+  uint32_t ci = cl;
+  unsigned long long mi = ml;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t cy = __shfl_up_sync(0xffffffffu, ci, o);
+    const unsigned long long my = __shfl_up_sync(0xffffffffu, mi, o);
+    if (lane >= o) {
+      ci += cy;
+      mi += my;
+    }
+  }
+  const unsigned long long ztot = __shfl_sync(0xffffffffu, mi, 31);
+  // integer sums reach tau * total exactly when they reach its ceiling
+  unsigned long long target;
   {
-    const unsigned long long qv = mass_of(V, smax);
+    const double tq = ceil(tau * (double)ztot);
+    target = tq >= (double)ztot ? ztot : (unsigned long long)tq;
+  }
+  const uint32_t kneed = (uint32_t)k_top;
+  uint32_t c_run = ci - cl;
+  unsigned long long m_run = mi - ml;
+  int hit = -1;
+  uint32_t hit_cb = 0u, hit_c = 0u;
+  unsigned long long hit_mb = 0ull;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (hit < 0 && c8[e] > 0u && c_run + c8[e] >= kneed && m_run + m8[e] >= target) {
+      hit = e;
+      hit_cb = c_run;
+      hit_mb = m_run;
+      hit_c = c8[e];
+    }
+    c_run += c8[e];
+    m_run += m8[e];
+  }
+  // both conditions hold once every block is counted (nb >= k, total >= target), so
+  // some lane hits; its bucket is the crossing one
+  const uint32_t hits = __ballot_sync(0xffffffffu, hit >= 0);
+  const int src = hits ? __ffs(hits) - 1 : 31;
+  const int bstar = __shfl_sync(0xffffffffu, kBins - 1 - 8 * lane - (hit < 0 ? 7 : hit), src);
+  const uint32_t above = __shfl_sync(0xffffffffu, hit_cb, src);
+  const unsigned long long above_m = __shfl_sync(0xffffffffu, hit_mb, src);
+  const uint32_t L = __shfl_sync(0xffffffffu, hit_c, src);
+
+  // ---- 3. the crossing bucket's blocks in index order; everything above is kept
+  uint32_t nc = 0u, kmin = 0xffffffffu, kmax = 0u;
+  for (int t0 = 0; t0 < nb; t0 += 32) {
+    const int t = t0 + lane;
+    int b = -1;
+    if (t < nb) b = bucket_of(sv[t], mn, scale);
+    if (b > bstar) kept[t] = 1;
+    const bool in = b == bstar;
+    const uint32_t bal = __ballot_sync(0xffffffffu, in);
+    if (in) {
+      cand[nc + __popc(bal & ((1u << lane) - 1u))] = t;
+      const uint32_t key = order_bits(sv[t]);
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+    }
+    nc += __popc(bal);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  __syncwarp();
+  // rank r of a candidate = candidates before it in (score desc, index asc) order;
+  // keep the r-th (0-based) and all before it for the smallest r that completes
+  // both conditions: take = r + 1
+  uint32_t best = L;  // take; L keeps the whole bucket (never needed when a lane hits)
+  if (kmin == kmax) {
+    // one score value: the order is the index order and every mass is equal
+    const unsigned long long qv = mass_of(sv[cand[0]], mx);
     const uint32_t tk = kneed > above ? kneed - above : 0u;
     uint32_t tm = 0u;
-    if ((double)above_m < target) {
-      tm = neq;
-      if (qv > 0ull) {
-        const double need = (target - (double)above_m) / (double)qv;
-        uint32_t t = (uint32_t)fmin(ceil(need), (double)neq);
-        // settle the rounding of the division on the integer sums themselves
-        while (t > 0u && (double)(above_m + (unsigned long long)(t - 1u) * qv) >= target) --t;
-        while (t < neq && (double)(above_m + (unsigned long long)t * qv) < target) ++t;
-        tm = t;
+    if (above_m < target) tm = qv > 0ull ? (uint32_t)min((unsigned long long)L, (target - above_m + qv - 1ull) / qv) : L;
+    best = min(L, max(tk, tm));
+  } else {
+    for (uint32_t c0 = 0; c0 < L; c0 += 32) {
+      const uint32_t c = c0 + lane;
+      uint32_t take = 0xffffffffu;
+      if (c < L) {
+        const int ti = cand[c];
+        const uint32_t key = order_bits(sv[ti]);
+        uint32_t rank = 0u;
+        unsigned long long pre = 0ull;
+        for (uint32_t d = 0; d < L; ++d) {
+          const int td = cand[d];
+          const float vd = sv[td];
+          const uint32_t kd = order_bits(vd);
+          if (kd > key || (kd == key && td < ti)) {
+            ++rank;
+            pre += mass_of(vd, mx);
+          }
+        }
+        if (above + rank + 1u >= kneed && above_m + pre + mass_of(sv[ti], mx) >= target) take = rank + 1u;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) take = min(take, __shfl_xor_sync(0xffffffffu, take, o));
+      best = min(best, take);
+    }
+    // mark the candidates whose rank is below `best`
+    for (uint32_t c0 = 0; c0 < L; c0 += 32) {
+      const uint32_t c = c0 + lane;
+      if (c < L) {
+        const int ti = cand[c];
+        const uint32_t key = order_bits(sv[ti]);
+        uint32_t rank = 0u;
+        for (uint32_t d = 0; d < L; ++d) {
+          const int td = cand[d];
+          const uint32_t kd = order_bits(sv[td]);
+          rank += (kd > key || (kd == key && td < ti)) ? 1u : 0u;
+        }
+        if (rank < best) kept[ti] = 1;
       }
     }
-    take = min(neq, max(tk, tm));
   }
+  if (kmin == kmax)
+    for (uint32_t c = lane; c < best; c += 32) kept[cand[c]] = 1;
+  __syncwarp();
 
-  // ---- compaction in ascending index order; each thread owns a contiguous run
-  const int per = (nb + kSelThreads - 1) / kSelThreads;
-  const int beg = min(nb, (int)threadIdx.x * per), end = min(nb, beg + per);
-  uint32_t n_tie = 0u, n_hi = 0u;
-  for (int t = beg; t < end; ++t) {
-    const uint32_t key = keys[t];
-    n_hi += key > V;
-    n_tie += key == V;
+  // ---- 4. ascending output
+  int32_t* out = idx + (size_t)row * nb;
+  uint32_t n = 0u;
+  for (int t0 = 0; t0 < nb; t0 += 32) {
+    const int t = t0 + lane;
+    const bool k = t < nb && kept[t];
+    const uint32_t bal = __ballot_sync(0xffffffffu, k);
+    if (k) out[n + __popc(bal & ((1u << lane) - 1u))] = t;
+    n += __popc(bal);
   }
-  // one scan of both counts, packed (each <= 4096)
-  uint32_t tot;
-  const uint32_t incl = block_incl_scan((n_tie << 16) | n_hi, sh.scan, &tot);
-  const uint32_t excl = incl - ((n_tie << 16) | n_hi);
-  const uint32_t tie_before = excl >> 16, hi_before = excl & 0xffffu;
-  uint32_t pos = hi_before + min(tie_before, take);
-  uint32_t tie_rank = tie_before;
-  int32_t* out = idx + row * nb;
-  for (int t = beg; t < end; ++t) {
-    const uint32_t key = keys[t];
-    if (key > V) {
-      out[pos++] = t;
-    } else if (key == V) {
-      if (tie_rank < take) out[pos++] = t;
-      ++tie_rank;
-    }
-  }
-  if (threadIdx.x == 0) counts[row] = (int32_t)((tot & 0xffffu) + take);
+  if (lane == 0) counts[row] = (int32_t)n;
 }
 
 }  // namespace
 
 cudaError_t select_launch(const float* scores, int Hh, int nb, int k_top, double tau, int32_t* counts, int32_t* idx,
                           cudaStream_t st) {
+  const size_t per = warp_bytes(nb);
+  int warps = (int)std::max<size_t>(1, std::min<size_t>(kSelWarpsMax, (200u * 1024u) / per));
+  const size_t smem = per * warps;
+  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int rows = Hh * nb;
   HookScope hs("select", st);
-  select_kernel<<<(unsigned)Hh * nb, kSelThreads, (size_t)nb * sizeof(uint32_t), st>>>(scores, nb, k_top, tau,
-                                                                                        counts, idx);
+  select_kernel<<<(unsigned)((rows + warps - 1) / warps), warps * 32, smem, st>>>(scores, rows, nb, k_top, tau,
+                                                                                 counts, idx);
   return cudaGetLastError();
 }
 
