@@ -39,13 +39,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSl2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
 constexpr float kScale = 0.08838834764831845f;                      // 1 / sqrt(128)
 
-__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) {  // K-major operand, K step kk (16 elems)
-  return smem_desc(tile + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-}
-__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int kk) {  // MN-major operand, K step kk (16 rows)
-  return smem_desc(tile + kk * 2048, kHalf, 1024, kSwizzle128B);
-}
-
 // ------------------------------------------------------------------- prep
 // 16 threads per (head, padded row), 8 channels (one 16-byte load of O and of dO) each.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
@@ -168,15 +161,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && cnt > 0) {
       constexpr uint32_t id_ss = idesc_bf16_f32(kB, kB, false, false);
       constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
-      const uint32_t qa = smem_u32(sm.q), da = smem_u32(sm.dO);
+      // tile descriptors, built once (K-major for S = Q K^T and dP = dO V^T, MN-major
+      // for K as the B operand of dQ += dS K); stages are kTile apart
+      const uint64_t dq_q = smem_desc(smem_u32(sm.q), 16, 1024, kSwizzle128B);
+      const uint64_t dq_do = smem_desc(smem_u32(sm.dO), 16, 1024, kSwizzle128B);
+      const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 16, 1024, kSwizzle128B);
+      const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), 16, 1024, kSwizzle128B);
+      const uint64_t dkmn0 = smem_desc(smem_u32(sm.k[0]), kHalf, 1024, kSwizzle128B);
+      auto koff = [](int kk) -> uint32_t { return (kk >> 2) * kHalf + (kk & 3) * 32; };
       bool ok = mbar_wait(smem_u32(&sm.q_full), 0, abort, status) &&
                 mbar_wait(smem_u32(&sm.kv_full[0]), 0, abort, status);
       if (ok) {
         tc_fence_after();
-        const uint32_t ka = smem_u32(sm.k[0]), va = smem_u32(sm.v[0]);
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, kdesc(qa, kk), kdesc(ka, kk), id_ss, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, desc_at(dq_q, koff(kk)), desc_at(dk0, koff(kk)), id_ss, kk > 0);
         tc_commit(smem_u32(&sm.s_full[0]));
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + 256, kdesc(da, kk), kdesc(va, kk), id_ss, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 256, desc_at(dq_do, koff(kk)), desc_at(dv0, koff(kk)), id_ss, kk > 0);
         tc_commit(smem_u32(&sm.dp_full));
       }
       for (int it = 0; ok && it < cnt; ++it) {
@@ -185,22 +187,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nst = (it + 1) & 1;
           if (!(ok = mbar_wait(smem_u32(&sm.kv_full[nst]), ((it + 1) >> 1) & 1, abort, status))) break;
           tc_fence_after();
-          const uint32_t ka = smem_u32(sm.k[nst]);
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + nst * 128, kdesc(qa, kk), kdesc(ka, kk), id_ss, kk > 0);
+          const uint64_t dk = desc_at(dk0, nst * kTile);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + nst * 128, desc_at(dq_q, koff(kk)), desc_at(dk, koff(kk)), id_ss, kk > 0);
           tc_commit(smem_u32(&sm.s_full[nst]));
         }
-        const uint32_t kt = smem_u32(sm.k[st]);
+        const uint64_t dkt = desc_at(dkmn0, st * kTile);
         if (!(ok = mbar_wait(smem_u32(&sm.ds_a[b]), (it >> 1) & 1, abort, status))) break;
         tc_fence_after();
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + 384, tmem + b * 128 + kk * 8, mndesc(kt, kk), id_ts, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + 384, tmem + b * 128 + kk * 8, desc_at(dkt, kk * 2048), id_ts, (it > 0 || kk > 0) ? 1u : 0u);
         if (!(ok = mbar_wait(smem_u32(&sm.ds_b[b]), (it >> 1) & 1, abort, status))) break;
         tc_fence_after();
-        for (int kk = 4; kk < 8; ++kk) mma_ts(tmem + 384, tmem + b * 128 + kk * 8, mndesc(kt, kk), id_ts, 1u);
+#pragma unroll
+        for (int kk = 4; kk < 8; ++kk) mma_ts(tmem + 384, tmem + b * 128 + kk * 8, desc_at(dkt, kk * 2048), id_ts, 1u);
         tc_commit(smem_u32(&sm.kv_empty[st]));
         if (it + 1 < cnt) {
-          const uint32_t va = smem_u32(sm.v[(it + 1) & 1]);
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + 256, kdesc(da, kk), kdesc(va, kk), id_ss, kk > 0);
+          const uint64_t dv = desc_at(dv0, ((it + 1) & 1) * kTile);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + 256, desc_at(dq_do, koff(kk)), desc_at(dv, koff(kk)), id_ss, kk > 0);
           tc_commit(smem_u32(&sm.dp_full));
         }
       }
@@ -391,28 +399,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && cnt > 0) {
       constexpr uint32_t id_ss = idesc_bf16_f32(kB, kB, false, false);
       constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
-      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
+      // tile descriptors, built once; the two query stages are sizeof(QdoStage) apart
+      const uint64_t dk_k = smem_desc(smem_u32(sm.k), 16, 1024, kSwizzle128B);
+      const uint64_t dk_v = smem_desc(smem_u32(sm.v), 16, 1024, kSwizzle128B);
+      const uint64_t dq0 = smem_desc(smem_u32(sm.st[0].q), 16, 1024, kSwizzle128B);
+      const uint64_t ddo0 = smem_desc(smem_u32(sm.st[0].dO), 16, 1024, kSwizzle128B);
+      const uint64_t dqmn0 = smem_desc(smem_u32(sm.st[0].q), kHalf, 1024, kSwizzle128B);
+      const uint64_t ddomn0 = smem_desc(smem_u32(sm.st[0].dO), kHalf, 1024, kSwizzle128B);
+      auto koff = [](int kk) -> uint32_t { return (kk >> 2) * kHalf + (kk & 3) * 32; };
       bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, abort, status);
       for (int it = 0; ok && it < cnt; ++it) {
         const int s = it & 1;
         if (!(ok = mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status))) break;
         tc_fence_after();
-        const uint32_t qa = smem_u32(sm.st[s].q), da = smem_u32(sm.st[s].dO);
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, kdesc(ka, kk), kdesc(qa, kk), id_ss, kk > 0);
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + 128, kdesc(va, kk), kdesc(da, kk), id_ss, kk > 0);
+        const uint32_t so = s * (uint32_t)sizeof(QdoStage);
+        const uint64_t dq = desc_at(dq0, so), ddo = desc_at(ddo0, so);
+        const uint64_t dqmn = desc_at(dqmn0, so), ddomn = desc_at(ddomn0, so);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, desc_at(dk_k, koff(kk)), desc_at(dq, koff(kk)), id_ss, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 128, desc_at(dk_v, koff(kk)), desc_at(ddo, koff(kk)), id_ss, kk > 0);
         tc_commit(smem_u32(&sm.sdp_full));
         if (!(ok = mbar_wait(smem_u32(&sm.half_a), it & 1, abort, status))) break;
         tc_fence_after();
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + 256, tmem + kk * 8, mndesc(da, kk), id_ts, acc);
-          mma_ts(tmem + 384, tmem + 128 + kk * 8, mndesc(qa, kk), id_ts, acc);
+          mma_ts(tmem + 256, tmem + kk * 8, desc_at(ddomn, kk * 2048), id_ts, acc);
+          mma_ts(tmem + 384, tmem + 128 + kk * 8, desc_at(dqmn, kk * 2048), id_ts, acc);
         }
         if (!(ok = mbar_wait(smem_u32(&sm.half_b), it & 1, abort, status))) break;
         tc_fence_after();
+#pragma unroll
         for (int kk = 4; kk < 8; ++kk) {
-          mma_ts(tmem + 256, tmem + kk * 8, mndesc(da, kk), id_ts, 1u);
-          mma_ts(tmem + 384, tmem + 128 + kk * 8, mndesc(qa, kk), id_ts, 1u);
+          mma_ts(tmem + 256, tmem + kk * 8, desc_at(ddomn, kk * 2048), id_ts, 1u);
+          mma_ts(tmem + 384, tmem + 128 + kk * 8, desc_at(dqmn, kk * 2048), id_ts, 1u);
         }
         tc_commit(smem_u32(&sm.qdo_empty[s]));
       }

@@ -219,19 +219,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && cnt > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, false, true);
-      const uint32_t qa = smem_u32(sm.q);
+      // tile descriptors, built once: Q and K K-major, V MN-major; stages are kTile apart
+      const uint64_t dq0 = smem_desc(smem_u32(sm.q), 16, 1024, kSwizzle128B);
+      const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 16, 1024, kSwizzle128B);
+      const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), kHalf, 1024, kSwizzle128B);
       bool ok = mbar_wait(smem_u32(&sm.q_full), 0, abort, status);
       for (int it = 0; ok && it <= cnt; ++it) {
         if (it < cnt) {
           const int st = it % kStages, b = it & 1;
           if (!mbar_wait(smem_u32(&sm.k_full[st]), (it / kStages) & 1, abort, status)) break;
           tc_fence_after();
-          const uint32_t ka = smem_u32(sm.k[st]);
+          const uint64_t dk = desc_at(dk0, st * kTile);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            mma_ss(tmem + b * 128, smem_desc(qa + off, 16, 1024, kSwizzle128B),
-                   smem_desc(ka + off, 16, 1024, kSwizzle128B), idesc_qk, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + b * 128, desc_at(dq0, off), desc_at(dk, off), idesc_qk, kk > 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(&sm.k_empty[st]));
           tc_commit(smem_u32(&sm.s_full[b]));
@@ -241,11 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(smem_u32(&sm.p_full[b]), (t >> 1) & 1, abort, status)) break;
           if (!mbar_wait(smem_u32(&sm.v_full[st]), (t / kStages) & 1, abort, status)) break;
           tc_fence_after();
-          const uint32_t va = smem_u32(sm.v[st]);
+          const uint64_t dv = desc_at(dv0, st * kTile);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
-            mma_ts(tmem + 256, tmem + b * 128 + kk * 8, smem_desc(va + kk * 2048, kHalf, 1024, kSwizzle128B),
-                   idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + 256, tmem + b * 128 + kk * 8, desc_at(dv, kk * 2048), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(smem_u32(&sm.v_empty[st]));
           tc_commit(smem_u32(&sm.o_bar));

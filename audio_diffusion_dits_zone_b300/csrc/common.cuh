@@ -175,6 +175,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 }
 constexpr uint32_t kSwizzle128B = 2;
 
+// The start-address field (bits [0,14), 16-byte units) of a descriptor moves to a
+// sub-tile by adding the byte offset / 16: shared addresses stay below 2^18, so the
+// field never carries into the offsets above it.  Building a descriptor takes
+// several dependent instructions; the MMA issuer builds one per tile up front and
+// reaches every k-step with this single add, which keeps one thread able to feed
+// the tensor pipe at its full rate.
+__device__ __forceinline__ uint64_t desc_at(uint64_t tile_desc, uint32_t byte_off) {
+  return tile_desc + (uint64_t)(byte_off >> 4);
+}
+
 // TMEM loads / stores, 32 lanes x 32 bits shape, 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
