@@ -7,19 +7,22 @@
 // token r of query block i and every token c of the kept blocks:
 //   O[r] = sum_c softmax_c(Q[r].K[c] / sqrt(d)) V[c],  lse[r] = log sum_c exp(Q[r].K[c] / sqrt(d)).
 //
-// One CTA per (head, query block), 7 warps with fixed roles:
+// One CTA per (head, query block), 8 warps with fixed roles:
 //   warp 0      TMA producer of K tiles (3-stage ring), walking the kept list;
 //   warp 6      TMA producer of the Q tile and of V tiles (3-stage ring);
-//   warp 1      TMEM owner and MMA issuer (one thread):
+//   warp 1      TMEM owner and S issuer (one thread):
 //                 S_b = Q K_j^T   (A, B from shared memory, K-major, 128B swizzle)
+//   warp 7      PV issuer (one thread):
 //                 O  += P_b V_j   (A = P from TMEM, B = V from shared memory, MN-major)
-//               S is double-buffered in TMEM so S(j+1) runs while the softmax of
-//               block j is computed; P (bf16) overwrites the S buffer it came from;
+//               S has three TMEM buffers: the S issuer runs up to three blocks
+//               ahead and overwrites buffer j % 3 only after PV(j-3), its last reader,
+//               has completed; the two issuers keep the tensor pipe supplied while the
+//               other waits; P (bf16) overwrites the S buffer it came from;
 //   warps 2-5   softmax: one thread per query row (its TMEM lane); online softmax in
 //               the log2 domain with ex2.approx; the O accumulator in TMEM is
 //               rescaled only when the running row max grows by more than 2^8
 //               (otherwise P is taken against the stale max, which bounds P by 256).
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384) of a 512-column allocation.
+// TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512).
 // The kept lists give block coordinates directly (tokens are already in block
 // order), so gathering a key block is one TMA box coordinate.  Every wait is
 // bounded; on a timeout the CTA drains its copies and MMAs, frees TMEM and exits
@@ -95,9 +98,11 @@ constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // key rows per tile
 constexpr int kD = 128;    // head dim
 constexpr int kStages = 3;
+constexpr int kSBuf = 3;                   // S buffers in TMEM
+constexpr uint32_t kOCol = 384;            // O accumulator columns [384, 512)
 constexpr uint32_t kHalf = 16384;          // one 128-row x 64-col bf16 box (128B swizzled)
 constexpr uint32_t kTile = 2 * kHalf;      // a 128 x 128 bf16 tile
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;  // 8 warps
 constexpr float kSl2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -109,8 +114,10 @@ struct FwdSmem {
   uint64_t q_full;
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_bar, mma_done;
+  uint64_t s_full[kSBuf], p_full[kSBuf];
+  uint64_t o_bar[2];           // PV(t) done, t even / odd
+  uint64_t pv_done[kSBuf];     // PV(t) done, t mod 3 (the S issuer may then overwrite buffer t mod 3)
+  uint64_t mma_done, s_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -148,12 +155,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.v_full[s]), 1);
       mbar_init(smem_u32(&sm.v_empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBuf; ++b) {
       mbar_init(smem_u32(&sm.s_full[b]), 1);
       mbar_init(smem_u32(&sm.p_full[b]), 4);
     }
-    mbar_init(smem_u32(&sm.o_bar), 1);
+    mbar_init(smem_u32(&sm.o_bar[0]), 1);
+    mbar_init(smem_u32(&sm.o_bar[1]), 1);
+    for (int b = 0; b < kSBuf; ++b) mbar_init(smem_u32(&sm.pv_done[b]), 1);
     mbar_init(smem_u32(&sm.mma_done), 1);
+    mbar_init(smem_u32(&sm.s_done), 1);
     sm.abort = 0;
     mbar_fence_init();
   }
@@ -215,44 +225,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // --------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- S issuer
+    // S(j) = Q K_j^T into TMEM buffer j % 3, as soon as K_j has landed and PV(j - 3),
+    // the last reader of that buffer, has completed.
     if (lane == 0 && cnt > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, false, true);
-      // tile descriptors, built once: Q and K K-major, V MN-major; stages are kTile apart
       const uint64_t dq0 = smem_desc(smem_u32(sm.q), 16, 1024, kSwizzle128B);
       const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 16, 1024, kSwizzle128B);
-      const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), kHalf, 1024, kSwizzle128B);
       bool ok = mbar_wait(smem_u32(&sm.q_full), 0, abort, status);
-      for (int it = 0; ok && it <= cnt; ++it) {
-        if (it < cnt) {
-          const int st = it % kStages, b = it & 1;
-          if (!mbar_wait(smem_u32(&sm.k_full[st]), (it / kStages) & 1, abort, status)) break;
-          tc_fence_after();
-          const uint64_t dk = desc_at(dk0, st * kTile);
+      for (int j = 0; ok && j < cnt; ++j) {
+        const int st = j % kStages, b = j % kSBuf;
+        if (j >= kSBuf && !(ok = mbar_wait(smem_u32(&sm.pv_done[b]), ((j / kSBuf) - 1) & 1, abort, status))) break;
+        if (!(ok = mbar_wait(smem_u32(&sm.k_full[st]), (j / kStages) & 1, abort, status))) break;
+        tc_fence_after();
+        const uint64_t dk = desc_at(dk0, st * kTile);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            mma_ss(tmem + b * 128, desc_at(dq0, off), desc_at(dk, off), idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&sm.k_empty[st]));
-          tc_commit(smem_u32(&sm.s_full[b]));
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          mma_ss(tmem + b * 128, desc_at(dq0, off), desc_at(dk, off), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        if (it >= 1) {
-          const int t = it - 1, b = t & 1, st = t % kStages;
-          if (!mbar_wait(smem_u32(&sm.p_full[b]), (t >> 1) & 1, abort, status)) break;
-          if (!mbar_wait(smem_u32(&sm.v_full[st]), (t / kStages) & 1, abort, status)) break;
-          tc_fence_after();
-          const uint64_t dv = desc_at(dv0, st * kTile);
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            mma_ts(tmem + 256, tmem + b * 128 + kk * 8, desc_at(dv, kk * 2048), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&sm.v_empty[st]));
-          tc_commit(smem_u32(&sm.o_bar));
-        }
+        tc_commit(smem_u32(&sm.k_empty[st]));
+        tc_commit(smem_u32(&sm.s_full[b]));
       }
-      // all MMAs of this CTA have completed once this barrier flips
+      tc_commit(smem_u32(&sm.s_done));
+      drain_wait(smem_u32(&sm.s_done), 0);
+    }
+  } else if (warp == 7) {
+    // --------------------------------------------------------------- PV issuer
+    // O += P(t) V_t as soon as the softmax has written P(t); a second issuing thread,
+    // so these products never queue behind the issue of an S product.
+    if (lane == 0 && cnt > 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kD, false, true);
+      const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), kHalf, 1024, kSwizzle128B);
+      bool ok = true;
+      for (int t = 0; ok && t < cnt; ++t) {
+        const int b = t % kSBuf, st = t % kStages;
+        if (!(ok = mbar_wait(smem_u32(&sm.p_full[b]), (t / kSBuf) & 1, abort, status))) break;
+        if (!(ok = mbar_wait(smem_u32(&sm.v_full[st]), (t / kStages) & 1, abort, status))) break;
+        tc_fence_after();
+        const uint64_t dv = desc_at(dv0, st * kTile);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + kOCol, tmem + b * 128 + kk * 8, desc_at(dv, kk * 2048), idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(smem_u32(&sm.v_empty[st]));
+        tc_commit(smem_u32(&sm.o_bar[t & 1]));
+        tc_commit(smem_u32(&sm.pv_done[b]));
+      }
+      // every PV has completed once this barrier flips; every S product completed
+      // before the softmax could write the P of the last block
       tc_commit(smem_u32(&sm.mma_done));
       drain_wait(smem_u32(&sm.mma_done), 0);
     }
@@ -263,13 +283,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
+    int j_next = cnt > 0 ? lst[0] : 0;  // block indices are read one block ahead
     for (int it = 0; it < cnt; ++it) {
-      const int b = it & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[b]), (it >> 1) & 1, abort, status));
+      const int b = it % kSBuf;
+      const int j_raw = j_next;
+      if (it + 1 < cnt) j_next = lst[it + 1];
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[b]), (it / kSBuf) & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
-      bool jok;
-      const int j = block_of(lst, it, nb, jok);
+      const bool jok = j_raw >= 0 && j_raw < nb;
+      const int j = jok ? j_raw : 0;
       const int len = jok ? min(kBN, N - j * kBN) : 0;
       if (!jok && r == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
       // the whole S row: four loads in flight, one wait
@@ -308,16 +331,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (m_new > m_used + kRescaleLog2) {
         const float alpha = fast_exp2(m_used - m_new);
         if (it > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_bar), (it - 1) & 1, abort, status));
+          // PV(it - 1) done; PV(it - 3) (same barrier, previous phase) completed before S(it)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&sm.o_bar[(it - 1) & 1]), ((it - 1) >> 1) & 1, abort, status));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t rr[32];
-            tmem_load_row32(lane_base + 256 + c4 * 32, rr);
+            tmem_load_row32(lane_base + kOCol + c4 * 32, rr);
 #pragma unroll
             for (int x = 0; x < 32; ++x) rr[x] = __float_as_uint(__uint_as_float(rr[x]) * alpha);
-            tmem_st32(lane_base + 256 + c4 * 32, rr);
+            tmem_st32(lane_base + kOCol + c4 * 32, rr);
           }
         }
         l *= alpha;
@@ -350,8 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = i * kBM + r;
     __nv_bfloat16* orow = o + (int64_t)row * ld + (int64_t)h * kD;
     if (ok && cnt > 0) {
-      // every MMA of the CTA has completed once mma_done flips; it completes once, so its
-      // parity cannot alias an older phase (o_bar may still be two phases behind here)
+      // every MMA of the CTA has completed once mma_done flips (it completes once)
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.mma_done), 0, abort, status));
       if (ok) {
         tc_fence_after();
@@ -359,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t rr[32];
-          tmem_load_row32(lane_base + 256 + c4 * 32, rr);
+          tmem_load_row32(lane_base + kOCol + c4 * 32, rr);
           uint32_t pk[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x)

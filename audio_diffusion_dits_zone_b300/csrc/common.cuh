@@ -60,11 +60,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition (no suspension, returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase of parity `parity` of barrier `bar` has completed.  Gives up
 // after `limit_ns` or as soon as another thread of the CTA has raised `*abort`;
-// on giving up it raises *abort, flags PRISM_DEV_TIMEOUT and returns false.
+// on giving up it raises *abort, flags PRISM_DEV_TIMEOUT and returns false.  A phase
+// that has already completed is seen by the non-blocking test without the potentially
+// suspending try_wait.
 __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, volatile int* abort,
                                                 uint32_t* status, uint64_t limit_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
