@@ -74,6 +74,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 }
 
 // --------------------------------------------------------------------- dQ
+// Warps: 0 TMA producer, 1 issuer of S and dP (TMEM owner), 10 issuer of dQ,
+// 2-5 softmax gradient of key columns 0-63 of every block, 6-9 of columns 64-127
+// (a thread owns one query row of one half).
+constexpr int kDqThreads = 352;
+
 struct DqSmem {
   uint8_t q[kTile];
   uint8_t dO[kTile];
@@ -81,16 +86,26 @@ struct DqSmem {
   uint8_t v[2][kTile];
   uint64_t q_full;
   uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full[2], dp_full;
-  uint64_t ds_a[2], ds_b[2];
-  uint64_t acc_done, mma_done;
+  uint64_t s_full[2], dp_full, dp_free;
+  uint64_t ds_full[2][2];  // [S buffer][key half]
+  uint64_t dq_done[2];     // dQ(t) has read S buffer t & 1
+  uint64_t acc_done, in_done;
   uint32_t tmem_base;
   int abort;
 };
 constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024;
 static_assert(kDqSmemBytes <= 232448, "shared memory budget");
 
-__global__ void __launch_bounds__(kThreads, 1)
+// TMEM: S0 [0,128) S1 [128,256) dP [256,384) dQ [384,512).
+// Two issuing threads:
+//   warp 1   dP(t+1) as soon as both halves have loaded dP(t) (dP is single-buffered),
+//            then S(t+1) into S buffer (t+1) & 1 once dQ(t-1), its last reader, has
+//            completed; so the next block's inputs are computed while block t's
+//            gradient is formed;
+//   warp 10  dQ(t) += dS(t) K_t in two K = 64 steps, one per key half, as soon as that
+//            half's warpgroup has written it;
+// dS (bf16) overwrites the S half it came from.
+__global__ void __launch_bounds__(kDqThreads, 1)
     bsa_dq_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                      const float* __restrict__ L2, const float* __restrict__ Dp, int npad,
@@ -110,12 +125,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.kv_full[s]), 1);
       mbar_init(smem_u32(&sm.kv_empty[s]), 1);
       mbar_init(smem_u32(&sm.s_full[s]), 1);
-      mbar_init(smem_u32(&sm.ds_a[s]), 4);
-      mbar_init(smem_u32(&sm.ds_b[s]), 4);
+      mbar_init(smem_u32(&sm.ds_full[s][0]), 4);
+      mbar_init(smem_u32(&sm.ds_full[s][1]), 4);
     }
     mbar_init(smem_u32(&sm.dp_full), 1);
+    mbar_init(smem_u32(&sm.dp_free), 8);
+    mbar_init(smem_u32(&sm.dq_done[0]), 1);
+    mbar_init(smem_u32(&sm.dq_done[1]), 1);
     mbar_init(smem_u32(&sm.acc_done), 1);
-    mbar_init(smem_u32(&sm.mma_done), 1);
+    mbar_init(smem_u32(&sm.in_done), 1);
     sm.abort = 0;
     mbar_fence_init();
   }
@@ -126,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;  // S0 [0,128) S1 [128,256) dP [256,384) dQ [384,512)
+  const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
   if (warp == 0) {
@@ -158,134 +176,147 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
+    // -------------------------------------------------- issuer of S and dP
     if (lane == 0 && cnt > 0) {
       constexpr uint32_t id_ss = idesc_bf16_f32(kB, kB, false, false);
-      constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
-      // tile descriptors, built once (K-major for S = Q K^T and dP = dO V^T, MN-major
-      // for K as the B operand of dQ += dS K); stages are kTile apart
       const uint64_t dq_q = smem_desc(smem_u32(sm.q), 16, 1024, kSwizzle128B);
       const uint64_t dq_do = smem_desc(smem_u32(sm.dO), 16, 1024, kSwizzle128B);
       const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 16, 1024, kSwizzle128B);
       const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), 16, 1024, kSwizzle128B);
-      const uint64_t dkmn0 = smem_desc(smem_u32(sm.k[0]), kHalf, 1024, kSwizzle128B);
       auto koff = [](int kk) -> uint32_t { return (kk >> 2) * kHalf + (kk & 3) * 32; };
+      auto issue_dp = [&](int st) {  // dP = dO V^T
+        const uint64_t dv = desc_at(dv0, st * kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + 256, desc_at(dq_do, koff(kk)), desc_at(dv, koff(kk)), id_ss, kk > 0);
+        tc_commit(smem_u32(&sm.dp_full));
+      };
+      auto issue_s = [&](int st, int b) {  // S = Q K^T
+        const uint64_t dk = desc_at(dk0, st * kTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + b * 128, desc_at(dq_q, koff(kk)), desc_at(dk, koff(kk)), id_ss, kk > 0);
+        tc_commit(smem_u32(&sm.s_full[b]));
+      };
       bool ok = mbar_wait(smem_u32(&sm.q_full), 0, abort, status) &&
                 mbar_wait(smem_u32(&sm.kv_full[0]), 0, abort, status);
       if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, desc_at(dq_q, koff(kk)), desc_at(dk0, koff(kk)), id_ss, kk > 0);
-        tc_commit(smem_u32(&sm.s_full[0]));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 256, desc_at(dq_do, koff(kk)), desc_at(dv0, koff(kk)), id_ss, kk > 0);
-        tc_commit(smem_u32(&sm.dp_full));
+        issue_s(0, 0);
+        issue_dp(0);
       }
+      for (int it = 0; ok && it + 1 < cnt; ++it) {
+        const int nb_ = (it + 1) & 1;  // stage and S buffer of block it + 1
+        if (!(ok = mbar_wait(smem_u32(&sm.dp_free), it & 1, abort, status))) break;
+        if (!(ok = mbar_wait(smem_u32(&sm.kv_full[nb_]), ((it + 1) >> 1) & 1, abort, status))) break;
+        tc_fence_after();
+        issue_dp(nb_);
+        if (it >= 1 && !(ok = mbar_wait(smem_u32(&sm.dq_done[nb_]), ((it - 1) >> 1) & 1, abort, status))) break;
+        tc_fence_after();
+        issue_s(nb_, nb_);
+      }
+      tc_commit(smem_u32(&sm.in_done));
+      drain_wait(smem_u32(&sm.in_done), 0);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ issuer of dQ
+    if (lane == 0 && cnt > 0) {
+      constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
+      const uint64_t dkmn0 = smem_desc(smem_u32(sm.k[0]), kHalf, 1024, kSwizzle128B);
+      bool ok = true;
       for (int it = 0; ok && it < cnt; ++it) {
         const int b = it & 1, st = it & 1;
-        if (it + 1 < cnt) {
-          const int nst = (it + 1) & 1;
-          if (!(ok = mbar_wait(smem_u32(&sm.kv_full[nst]), ((it + 1) >> 1) & 1, abort, status))) break;
-          tc_fence_after();
-          const uint64_t dk = desc_at(dk0, nst * kTile);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + nst * 128, desc_at(dq_q, koff(kk)), desc_at(dk, koff(kk)), id_ss, kk > 0);
-          tc_commit(smem_u32(&sm.s_full[nst]));
-        }
         const uint64_t dkt = desc_at(dkmn0, st * kTile);
-        if (!(ok = mbar_wait(smem_u32(&sm.ds_a[b]), (it >> 1) & 1, abort, status))) break;
-        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + 384, tmem + b * 128 + kk * 8, desc_at(dkt, kk * 2048), id_ts, (it > 0 || kk > 0) ? 1u : 0u);
-        if (!(ok = mbar_wait(smem_u32(&sm.ds_b[b]), (it >> 1) & 1, abort, status))) break;
-        tc_fence_after();
+        for (int half = 0; half < 2; ++half) {
+          if (!(ok = mbar_wait(smem_u32(&sm.ds_full[b][half]), (it >> 1) & 1, abort, status))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 4; kk < 8; ++kk) mma_ts(tmem + 384, tmem + b * 128 + kk * 8, desc_at(dkt, kk * 2048), id_ts, 1u);
-        tc_commit(smem_u32(&sm.kv_empty[st]));
-        if (it + 1 < cnt) {
-          const uint64_t dv = desc_at(dv0, ((it + 1) & 1) * kTile);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + 256, desc_at(dq_do, koff(kk)), desc_at(dv, koff(kk)), id_ss, kk > 0);
-          tc_commit(smem_u32(&sm.dp_full));
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + 384, tmem + b * 128 + half * 64 + kk * 8, desc_at(dkt, (half * 4 + kk) * 2048), id_ts,
+                   (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
         }
+        if (!ok) break;
+        tc_commit(smem_u32(&sm.kv_empty[st]));
+        tc_commit(smem_u32(&sm.dq_done[b]));
       }
+      // every dQ product has completed once this barrier flips; every S and dP product
+      // completed before the softmax could write the last block's dS
       tc_commit(smem_u32(&sm.acc_done));
-      tc_commit(smem_u32(&sm.mma_done));
-      drain_wait(smem_u32(&sm.mma_done), 0);
+      drain_wait(smem_u32(&sm.acc_done), 0);
     }
-  } else if (warp >= 2) {
+  } else {
+    const int half = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
+    const int c0 = half * 64;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const int row = i * kB + r;
     const float l2 = L2[(size_t)h * npad + row];
     const float dr = Dp[(size_t)h * npad + row];
     bool ok = true;
+    int j_next = cnt > 0 ? lst[0] : 0;  // block indices are read one block ahead
     for (int it = 0; it < cnt; ++it) {
       const int b = it & 1;
+      const int j = j_next;
+      if (it + 1 < cnt) j_next = lst[it + 1];
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[b]), (it >> 1) & 1, abort, status) &&
                                        mbar_wait(smem_u32(&sm.dp_full), it & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
-      int j = lst[it];
       const int len = (j >= 0 && j < nb) ? min(kB, N - j * kB) : 0;
+      uint32_t s0[32], s1[32], d0[32], d1[32];
+      tmem_ld32(lane_base + b * 128 + c0, s0);
+      tmem_ld32(lane_base + b * 128 + c0 + 32, s1);
+      tmem_ld32(lane_base + 256 + c0, d0);
+      tmem_ld32(lane_base + 256 + c0 + 32, d1);
+      tmem_wait_ld();
+      reg_fence(s0);
+      reg_fence(s1);
+      reg_fence(d0);
+      reg_fence(d1);
+      // dP is in registers: the next block's dO V^T may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.dp_free));
+      if (len < c0 + 64) {  // short or skipped key block (warp-uniform): masked keys get P = 0
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t s0[32], s1[32], d0[32], d1[32];
-        tmem_ld32(lane_base + b * 128 + half * 64, s0);
-        tmem_ld32(lane_base + b * 128 + half * 64 + 32, s1);
-        tmem_ld32(lane_base + 256 + half * 64, d0);
-        tmem_ld32(lane_base + 256 + half * 64 + 32, d1);
-        tmem_wait_ld();
-        reg_fence(s0);
-        reg_fence(s1);
-        reg_fence(d0);
-        reg_fence(d1);
-        if (len < kB) {  // short or skipped key block (warp-uniform): masked keys get P = 0
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            if (half * 64 + x >= len) s0[x] = __float_as_uint(-INFINITY);
-            if (half * 64 + 32 + x >= len) s1[x] = __float_as_uint(-INFINITY);
-          }
+        for (int x = 0; x < 32; ++x) {
+          if (c0 + x >= len) s0[x] = __float_as_uint(-INFINITY);
+          if (c0 + 32 + x >= len) s1[x] = __float_as_uint(-INFINITY);
         }
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c4 = half * 2 + cc;
-          const uint32_t* sr = cc ? s1 : s0;
-          const uint32_t* pr = cc ? d1 : d0;
-          uint32_t pk[16];
-#pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * x]), kSl2, -l2));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * x + 1]), kSl2, -l2));
-            pk[x] = pack_bf16x2(p0 * (__uint_as_float(pr[2 * x]) - dr), p1 * (__uint_as_float(pr[2 * x + 1]) - dr));
-          }
-          tmem_st16(lane_base + b * 128 + c4 * 16, pk);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(half == 0 ? &sm.ds_a[b] : &sm.ds_b[b]));
       }
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const uint32_t* sr = cc ? s1 : s0;
+        const uint32_t* pr = cc ? d1 : d0;
+        uint32_t pk[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * x]), kSl2, -l2));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * x + 1]), kSl2, -l2));
+          pk[x] = pack_bf16x2(p0 * (__uint_as_float(pr[2 * x]) - dr), p1 * (__uint_as_float(pr[2 * x + 1]) - dr));
+        }
+        tmem_st16(lane_base + b * 128 + c0 + cc * 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.ds_full[b][half]));
     }
-    __nv_bfloat16* out = dq + (int64_t)row * ld + (int64_t)h * kD;
+    __nv_bfloat16* out = dq + (int64_t)row * ld + (int64_t)h * kD + c0;
     if (ok && cnt > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_done), 0, abort, status));
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c2 = 0; c2 < 2; ++c2) {
           uint32_t rr[32];
-          tmem_load_row32(lane_base + 384 + c4 * 32, rr);
+          tmem_load_row32(lane_base + 384 + c0 + c2 * 32, rr);
           uint32_t pk[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x)
             pk[x] = pack_bf16x2(__uint_as_float(rr[2 * x]) * kScale, __uint_as_float(rr[2 * x + 1]) * kScale);
           if (row < N) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c4 * 32);
+            uint4* dst = reinterpret_cast<uint4*>(out + c2 * 32);
 #pragma unroll
             for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
           }
@@ -294,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (cnt == 0 && row < N) {
       uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
-      for (int x = 0; x < 16; ++x) dst[x] = make_uint4(0u, 0u, 0u, 0u);
+      for (int x = 0; x < 8; ++x) dst[x] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   tc_fence_before();
@@ -306,6 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------- dK dV
+// Warps: 0 TMA producer, 1 issuer of S^T and dP^T (TMEM owner), 10 issuer of dV and
+// dK, 2-5 softmax gradient of query columns 0-63 of every query block, 6-9 of
+// columns 64-127; a thread owns one key row (its TMEM lane) of one half.
+constexpr int kDkdvThreads = 352;
+
 struct QdoStage {
   uint8_t q[kTile];
   uint8_t dO[kTile];
@@ -318,8 +354,10 @@ struct DkdvSmem {
   float dr[2][kB];  // D of the stage's query rows
   uint64_t kv_full;
   uint64_t qdo_full[2], qdo_empty[2];
-  uint64_t sdp_full, half_a, half_b;
-  uint64_t acc_done, mma_done;
+  uint64_t sdp_full[2];  // [query half]: S^T and dP^T of that half computed
+  uint64_t pds_full[2];  // [query half]: P^T and dS^T of that half written
+  uint64_t vk_done[2];   // [query half]: dV and dK have read that half's P^T and dS^T
+  uint64_t acc_done, in_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -327,7 +365,16 @@ constexpr size_t kDkdvSmemBytes = sizeof(DkdvSmem) + 1024;
 static_assert(kDkdvSmemBytes <= 232448, "shared memory budget");
 static_assert(sizeof(QdoStage) % 1024 == 0, "stages keep 1024-byte alignment for the swizzled tiles");
 
-__global__ void __launch_bounds__(kThreads, 1)
+// TMEM: S^T_a [0,64) S^T_b [64,128) dP^T_a [128,192) dP^T_b [192,256) dV [256,384)
+// dK [384,512); half a = query rows 0-63 of the query block, half b = rows 64-127.
+// Per query half x and pair t:  S^T_x = K Q_x^T and dP^T_x = V dO_x^T (N = 64);
+// the half's warpgroup writes P^T_x (bf16) over the first 32 columns of S^T_x and
+// dS^T_x over the first 32 of dP^T_x; dV += P^T_x dO_x and dK += dS^T_x Q_x (K = 64).
+// Two issuing threads: warp 10 issues dV/dK of a half as soon as it is written;
+// warp 1 issues the next pair's S^T_x, dP^T_x once those dV/dK products have
+// completed.  The halves alternate in the tensor pipe, so one half's products run
+// while the other half's softmax gradient is computed.
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     bsa_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                        const float* __restrict__ L2, const float* __restrict__ Dp, int npad,
@@ -346,12 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sm.qdo_full[s]), 1);
       mbar_init(smem_u32(&sm.qdo_empty[s]), 1);
+      mbar_init(smem_u32(&sm.sdp_full[s]), 1);
+      mbar_init(smem_u32(&sm.pds_full[s]), 4);
+      mbar_init(smem_u32(&sm.vk_done[s]), 1);
     }
-    mbar_init(smem_u32(&sm.sdp_full), 1);
-    mbar_init(smem_u32(&sm.half_a), 4);
-    mbar_init(smem_u32(&sm.half_b), 4);
     mbar_init(smem_u32(&sm.acc_done), 1);
-    mbar_init(smem_u32(&sm.mma_done), 1);
+    mbar_init(smem_u32(&sm.in_done), 1);
     sm.abort = 0;
     mbar_fence_init();
   }
@@ -362,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = sm.tmem_base;  // S^T [0,128) dP^T [128,256) dV [256,384) dK [384,512)
+  const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
 
   if (warp == 0) {
@@ -396,129 +443,139 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
+    // ------------------------------------------------ issuer of S^T and dP^T
     if (lane == 0 && cnt > 0) {
-      constexpr uint32_t id_ss = idesc_bf16_f32(kB, kB, false, false);
-      constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
-      // tile descriptors, built once; the two query stages are sizeof(QdoStage) apart
+      constexpr uint32_t id_h = idesc_bf16_f32(kB, 64, false, false);  // M = 128 keys, N = 64 queries
       const uint64_t dk_k = smem_desc(smem_u32(sm.k), 16, 1024, kSwizzle128B);
       const uint64_t dk_v = smem_desc(smem_u32(sm.v), 16, 1024, kSwizzle128B);
       const uint64_t dq0 = smem_desc(smem_u32(sm.st[0].q), 16, 1024, kSwizzle128B);
       const uint64_t ddo0 = smem_desc(smem_u32(sm.st[0].dO), 16, 1024, kSwizzle128B);
-      const uint64_t dqmn0 = smem_desc(smem_u32(sm.st[0].q), kHalf, 1024, kSwizzle128B);
-      const uint64_t ddomn0 = smem_desc(smem_u32(sm.st[0].dO), kHalf, 1024, kSwizzle128B);
       auto koff = [](int kk) -> uint32_t { return (kk >> 2) * kHalf + (kk & 3) * 32; };
       bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, abort, status);
       for (int it = 0; ok && it < cnt; ++it) {
         const int s = it & 1;
         if (!(ok = mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status))) break;
-        tc_fence_after();
         const uint32_t so = s * (uint32_t)sizeof(QdoStage);
-        const uint64_t dq = desc_at(dq0, so), ddo = desc_at(ddo0, so);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          // the half's rows of the Q / dO tiles start 64 rows (8 KB) into each box
+          const uint64_t dq = desc_at(dq0, so + half * 8192), ddo = desc_at(ddo0, so + half * 8192);
+          if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.vk_done[half]), (it - 1) & 1, abort, status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + half * 64, desc_at(dk_k, koff(kk)), desc_at(dq, koff(kk)), id_h, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + 128 + half * 64, desc_at(dk_v, koff(kk)), desc_at(ddo, koff(kk)), id_h, kk > 0);
+          tc_commit(smem_u32(&sm.sdp_full[half]));
+        }
+      }
+      tc_commit(smem_u32(&sm.in_done));
+      drain_wait(smem_u32(&sm.in_done), 0);
+    }
+  } else if (warp == 10) {
+    // -------------------------------------------------- issuer of dV and dK
+    if (lane == 0 && cnt > 0) {
+      constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
+      const uint64_t dqmn0 = smem_desc(smem_u32(sm.st[0].q), kHalf, 1024, kSwizzle128B);
+      const uint64_t ddomn0 = smem_desc(smem_u32(sm.st[0].dO), kHalf, 1024, kSwizzle128B);
+      bool ok = true;
+      for (int it = 0; ok && it < cnt; ++it) {
+        const int s = it & 1;
+        const uint32_t so = s * (uint32_t)sizeof(QdoStage);
         const uint64_t dqmn = desc_at(dqmn0, so), ddomn = desc_at(ddomn0, so);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, desc_at(dk_k, koff(kk)), desc_at(dq, koff(kk)), id_ss, kk > 0);
+        for (int half = 0; half < 2; ++half) {
+          if (!(ok = mbar_wait(smem_u32(&sm.pds_full[half]), it & 1, abort, status))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 128, desc_at(dk_v, koff(kk)), desc_at(ddo, koff(kk)), id_ss, kk > 0);
-        tc_commit(smem_u32(&sm.sdp_full));
-        if (!(ok = mbar_wait(smem_u32(&sm.half_a), it & 1, abort, status))) break;
-        tc_fence_after();
+          for (int kk = 0; kk < 4; ++kk)  // dV += P^T_x dO_x
+            mma_ts(tmem + 256, tmem + half * 64 + kk * 8, desc_at(ddomn, (half * 4 + kk) * 2048), id_ts,
+                   (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + 256, tmem + kk * 8, desc_at(ddomn, kk * 2048), id_ts, acc);
-          mma_ts(tmem + 384, tmem + 128 + kk * 8, desc_at(dqmn, kk * 2048), id_ts, acc);
+          for (int kk = 0; kk < 4; ++kk)  // dK += dS^T_x Q_x
+            mma_ts(tmem + 384, tmem + 128 + half * 64 + kk * 8, desc_at(dqmn, (half * 4 + kk) * 2048), id_ts,
+                   (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&sm.vk_done[half]));
         }
-        if (!(ok = mbar_wait(smem_u32(&sm.half_b), it & 1, abort, status))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 4; kk < 8; ++kk) {
-          mma_ts(tmem + 256, tmem + kk * 8, desc_at(ddomn, kk * 2048), id_ts, 1u);
-          mma_ts(tmem + 384, tmem + 128 + kk * 8, desc_at(dqmn, kk * 2048), id_ts, 1u);
-        }
+        if (!ok) break;
         tc_commit(smem_u32(&sm.qdo_empty[s]));
       }
+      // every dV / dK product has completed once this barrier flips; every S^T and dP^T
+      // product completed before the softmax could write the last pair's P^T, dS^T
       tc_commit(smem_u32(&sm.acc_done));
-      tc_commit(smem_u32(&sm.mma_done));
-      drain_wait(smem_u32(&sm.mma_done), 0);
+      drain_wait(smem_u32(&sm.acc_done), 0);
     }
-  } else if (warp >= 2) {
+  } else {
+    const int half = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int c = quarter * 32 + lane;  // key row of block j = TMEM lane
+    const int q0 = half * 64;           // this thread's query columns q0 .. q0 + 63
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     bool ok = true;
     for (int it = 0; it < cnt; ++it) {
       const int s = it & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status) &&
-                                       mbar_wait(smem_u32(&sm.sdp_full), it & 1, abort, status));
+                                       mbar_wait(smem_u32(&sm.sdp_full[half]), it & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
-      const float4* l2v = reinterpret_cast<const float4*>(sm.l2[s]);
-      const float4* drv = reinterpret_cast<const float4*>(sm.dr[s]);
+      const float4* l2v = reinterpret_cast<const float4*>(sm.l2[s] + q0);
+      const float4* drv = reinterpret_cast<const float4*>(sm.dr[s] + q0);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        // two 32-column chunks of S^T and dP^T in flight, one wait
-        uint32_t s0[32], s1[32], d0[32], d1[32];
-        tmem_ld32(lane_base + half * 64, s0);
-        tmem_ld32(lane_base + half * 64 + 32, s1);
-        tmem_ld32(lane_base + 128 + half * 64, d0);
-        tmem_ld32(lane_base + 128 + half * 64 + 32, d1);
+      for (int cc = 0; cc < 2; ++cc) {  // 32 query columns at a time
+        uint32_t sr[32], pr[32];
+        tmem_ld32(lane_base + q0 + cc * 32, sr);
+        tmem_ld32(lane_base + 128 + q0 + cc * 32, pr);
         tmem_wait_ld();
-        reg_fence(s0);
-        reg_fence(s1);
-        reg_fence(d0);
-        reg_fence(d1);
+        reg_fence(sr);
+        reg_fence(pr);
+        uint32_t pp[16], dd[16];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c4 = half * 2 + cc;
-          const uint32_t* sr = cc ? s1 : s0;
-          const uint32_t* pr = cc ? d1 : d0;
-          uint32_t pp[16], dd[16];
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {  // 4 query columns per vector load of the row statistics
-            const float4 L = l2v[c4 * 8 + q4];
-            const float4 Dv = drv[c4 * 8 + q4];
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4]), kSl2, -L.x));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 1]), kSl2, -L.y));
-            const float p2 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 2]), kSl2, -L.z));
-            const float p3 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 3]), kSl2, -L.w));
-            pp[2 * q4] = pack_bf16x2(p0, p1);
-            pp[2 * q4 + 1] = pack_bf16x2(p2, p3);
-            dd[2 * q4] = pack_bf16x2(p0 * (__uint_as_float(pr[4 * q4]) - Dv.x),
-                                     p1 * (__uint_as_float(pr[4 * q4 + 1]) - Dv.y));
-            dd[2 * q4 + 1] = pack_bf16x2(p2 * (__uint_as_float(pr[4 * q4 + 2]) - Dv.z),
-                                         p3 * (__uint_as_float(pr[4 * q4 + 3]) - Dv.w));
-          }
-          tmem_st16(lane_base + c4 * 16, pp);
-          tmem_st16(lane_base + 128 + c4 * 16, dd);
+        for (int q4 = 0; q4 < 8; ++q4) {  // 4 query columns per vector load of the row statistics
+          const float4 L = l2v[cc * 8 + q4];
+          const float4 Dv = drv[cc * 8 + q4];
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4]), kSl2, -L.x));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 1]), kSl2, -L.y));
+          const float p2 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 2]), kSl2, -L.z));
+          const float p3 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 3]), kSl2, -L.w));
+          pp[2 * q4] = pack_bf16x2(p0, p1);
+          pp[2 * q4 + 1] = pack_bf16x2(p2, p3);
+          dd[2 * q4] = pack_bf16x2(p0 * (__uint_as_float(pr[4 * q4]) - Dv.x), p1 * (__uint_as_float(pr[4 * q4 + 1]) - Dv.y));
+          dd[2 * q4 + 1] =
+              pack_bf16x2(p2 * (__uint_as_float(pr[4 * q4 + 2]) - Dv.z), p3 * (__uint_as_float(pr[4 * q4 + 3]) - Dv.w));
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(half == 0 ? &sm.half_a : &sm.half_b));
+        // P^T_x over the first 32 columns of S^T_x, dS^T_x over the first 32 of dP^T_x
+        // (this chunk's columns were read above; the writes land in columns already read)
+        tmem_st16(lane_base + q0 + cc * 16, pp);
+        tmem_st16(lane_base + 128 + q0 + cc * 16, dd);
       }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.pds_full[half]));
     }
     const int col = j * kB + c;
-    __nv_bfloat16* dk_row = dk + (int64_t)col * ld + (int64_t)h * kD;
-    __nv_bfloat16* dv_row = dv + (int64_t)col * ld + (int64_t)h * kD;
+    __nv_bfloat16* dk_row = dk + (int64_t)col * ld + (int64_t)h * kD + q0;
+    __nv_bfloat16* dv_row = dv + (int64_t)col * ld + (int64_t)h * kD + q0;
     if (ok && cnt > 0) {
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_done), 0, abort, status));
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          __nv_bfloat16* out = half ? dk_row : dv_row;
-          const float sc = half ? kScale : 1.f;
+        for (int which = 0; which < 2; ++which) {  // dV, then dK (scaled by 1/sqrt(d))
+          __nv_bfloat16* out = which ? dk_row : dv_row;
+          const float sc = which ? kScale : 1.f;
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
+          for (int c2 = 0; c2 < 2; ++c2) {
             uint32_t rr[32];
-            tmem_load_row32(lane_base + 256 + half * 128 + c4 * 32, rr);
+            tmem_load_row32(lane_base + 256 + which * 128 + q0 + c2 * 32, rr);
             uint32_t pk[16];
 #pragma unroll
             for (int x = 0; x < 16; ++x)
               pk[x] = pack_bf16x2(__uint_as_float(rr[2 * x]) * sc, __uint_as_float(rr[2 * x + 1]) * sc);
             if (col < N) {
-              uint4* dst = reinterpret_cast<uint4*>(out + c4 * 32);
+              uint4* dst = reinterpret_cast<uint4*>(out + c2 * 32);
 #pragma unroll
               for (int x = 0; x < 4; ++x)
                 dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
@@ -530,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4* a = reinterpret_cast<uint4*>(dk_row);
       uint4* b = reinterpret_cast<uint4*>(dv_row);
 #pragma unroll
-      for (int x = 0; x < 16; ++x) a[x] = b[x] = make_uint4(0u, 0u, 0u, 0u);
+      for (int x = 0; x < 8; ++x) a[x] = b[x] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   tc_fence_before();
@@ -575,12 +632,12 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
     return e;
   {
     HookScope hs("bsa_dq_tc", st);
-    bsa_dq_tc_kernel<<<(unsigned)Hh * nb, kThreads, kDqSmemBytes, st>>>(
+    bsa_dq_tc_kernel<<<(unsigned)Hh * nb, kDqThreads, kDqSmemBytes, st>>>(
         mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dq), ld, N, counts, idx, nb, status);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   HookScope hs("bsa_dkdv_tc", st);
-  bsa_dkdv_tc_kernel<<<(unsigned)Hh * nb, kThreads, kDkdvSmemBytes, st>>>(
+  bsa_dkdv_tc_kernel<<<(unsigned)Hh * nb, kDkdvThreads, kDkdvSmemBytes, st>>>(
       mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), ld, N,
       tcounts, tidx, nb, status);
   return cudaGetLastError();
