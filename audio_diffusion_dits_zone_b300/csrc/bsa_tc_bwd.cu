@@ -79,13 +79,15 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 // (a thread owns one query row of one half).
 constexpr int kDqThreads = 352;
 
+constexpr int kDqKStages = 3, kDqVStages = 2;
 struct DqSmem {
   uint8_t q[kTile];
   uint8_t dO[kTile];
-  uint8_t k[2][kTile];
-  uint8_t v[2][kTile];
+  uint8_t k[kDqKStages][kTile];
+  uint8_t v[kDqVStages][kTile];
   uint64_t q_full;
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full[kDqKStages], k_empty[kDqKStages];  // K_t: read by S(t) and dQ(t)
+  uint64_t v_full[kDqVStages], v_empty[kDqVStages];  // V_t: read by dP(t) only
   uint64_t s_full[2], dp_full, dp_free;
   uint64_t ds_full[2][2];  // [S buffer][key half]
   uint64_t dq_done[2];     // dQ(t) has read S buffer t & 1
@@ -121,9 +123,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int32_t* lst = idx + (size_t)item * nb;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
+    for (int s = 0; s < kDqKStages; ++s) {
+      mbar_init(smem_u32(&sm.k_full[s]), 1);
+      mbar_init(smem_u32(&sm.k_empty[s]), 1);
+    }
+    for (int s = 0; s < kDqVStages; ++s) {
+      mbar_init(smem_u32(&sm.v_full[s]), 1);
+      mbar_init(smem_u32(&sm.v_empty[s]), 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&sm.kv_full[s]), 1);
-      mbar_init(smem_u32(&sm.kv_empty[s]), 1);
       mbar_init(smem_u32(&sm.s_full[s]), 1);
       mbar_init(smem_u32(&sm.ds_full[s][0]), 4);
       mbar_init(smem_u32(&sm.ds_full[s][1]), 4);
@@ -155,24 +163,32 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tma_load_2d(smem_u32(sm.q) + kHalf, &tmq, h * kD + 64, i * kB, qb);
       tma_load_2d(smem_u32(sm.dO), &tmdo, h * kD, i * kB, qb);
       tma_load_2d(smem_u32(sm.dO) + kHalf, &tmdo, h * kD + 64, i * kB, qb);
-      int armed[2] = {0, 0};
+      // K and V in separate rings: V_t is free once dP(t) has completed, K_t only once
+      // dQ(t) has, so V can run further ahead than K
+      int karmed[kDqKStages] = {0, 0, 0}, varmed[kDqVStages] = {0, 0};
       for (int it = 0; it < cnt; ++it) {
-        const int st = it & 1;
-        if (it >= 2 && !mbar_wait(smem_u32(&sm.kv_empty[st]), ((it >> 1) - 1) & 1, abort, status)) break;
+        const int ks = it % kDqKStages, vs = it % kDqVStages;
         int j = lst[it];
         if (j < 0 || j >= nb) j = 0;
-        const uint32_t bar = smem_u32(&sm.kv_full[st]);
-        mbar_arrive_expect_tx(bar, 2 * kTile);
-        tma_load_2d(smem_u32(sm.k[st]), &tmk, h * kD, j * kB, bar);
-        tma_load_2d(smem_u32(sm.k[st]) + kHalf, &tmk, h * kD + 64, j * kB, bar);
-        tma_load_2d(smem_u32(sm.v[st]), &tmv, h * kD, j * kB, bar);
-        tma_load_2d(smem_u32(sm.v[st]) + kHalf, &tmv, h * kD + 64, j * kB, bar);
-        ++armed[st];
+        if (it >= kDqVStages && !mbar_wait(smem_u32(&sm.v_empty[vs]), ((it / kDqVStages) - 1) & 1, abort, status)) break;
+        const uint32_t vbar = smem_u32(&sm.v_full[vs]);
+        mbar_arrive_expect_tx(vbar, kTile);
+        tma_load_2d(smem_u32(sm.v[vs]), &tmv, h * kD, j * kB, vbar);
+        tma_load_2d(smem_u32(sm.v[vs]) + kHalf, &tmv, h * kD + 64, j * kB, vbar);
+        ++varmed[vs];
+        if (it >= kDqKStages && !mbar_wait(smem_u32(&sm.k_empty[ks]), ((it / kDqKStages) - 1) & 1, abort, status)) break;
+        const uint32_t kbar = smem_u32(&sm.k_full[ks]);
+        mbar_arrive_expect_tx(kbar, kTile);
+        tma_load_2d(smem_u32(sm.k[ks]), &tmk, h * kD, j * kB, kbar);
+        tma_load_2d(smem_u32(sm.k[ks]) + kHalf, &tmk, h * kD + 64, j * kB, kbar);
+        ++karmed[ks];
       }
       if (*abort) {
         drain_wait(qb, 0);
-        for (int s = 0; s < 2; ++s)
-          if (armed[s]) drain_wait(smem_u32(&sm.kv_full[s]), (armed[s] - 1) & 1);
+        for (int s = 0; s < kDqKStages; ++s)
+          if (karmed[s]) drain_wait(smem_u32(&sm.k_full[s]), (karmed[s] - 1) & 1);
+        for (int s = 0; s < kDqVStages; ++s)
+          if (varmed[s]) drain_wait(smem_u32(&sm.v_full[s]), (varmed[s] - 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -184,34 +200,39 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 16, 1024, kSwizzle128B);
       const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), 16, 1024, kSwizzle128B);
       auto koff = [](int kk) -> uint32_t { return (kk >> 2) * kHalf + (kk & 3) * 32; };
-      auto issue_dp = [&](int st) {  // dP = dO V^T
-        const uint64_t dv = desc_at(dv0, st * kTile);
+      auto issue_dp = [&](int t) {  // dP(t) = dO V_t^T; V_t's stage is free once it completes
+        const int vs = t % kDqVStages;
+        const uint64_t dv = desc_at(dv0, vs * kTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + 256, desc_at(dq_do, koff(kk)), desc_at(dv, koff(kk)), id_ss, kk > 0);
         tc_commit(smem_u32(&sm.dp_full));
+        tc_commit(smem_u32(&sm.v_empty[vs]));
       };
-      auto issue_s = [&](int st, int b) {  // S = Q K^T
-        const uint64_t dk = desc_at(dk0, st * kTile);
+      auto issue_s = [&](int t) {  // S(t) = Q K_t^T into S buffer t & 1
+        const uint64_t dk = desc_at(dk0, (t % kDqKStages) * kTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + b * 128, desc_at(dq_q, koff(kk)), desc_at(dk, koff(kk)), id_ss, kk > 0);
-        tc_commit(smem_u32(&sm.s_full[b]));
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + (t & 1) * 128, desc_at(dq_q, koff(kk)), desc_at(dk, koff(kk)), id_ss, kk > 0);
+        tc_commit(smem_u32(&sm.s_full[t & 1]));
       };
       bool ok = mbar_wait(smem_u32(&sm.q_full), 0, abort, status) &&
-                mbar_wait(smem_u32(&sm.kv_full[0]), 0, abort, status);
+                mbar_wait(smem_u32(&sm.v_full[0]), 0, abort, status) &&
+                mbar_wait(smem_u32(&sm.k_full[0]), 0, abort, status);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
         issue_dp(0);
+        issue_s(0);
       }
       for (int it = 0; ok && it + 1 < cnt; ++it) {
-        const int nb_ = (it + 1) & 1;  // stage and S buffer of block it + 1
+        const int t = it + 1;
         if (!(ok = mbar_wait(smem_u32(&sm.dp_free), it & 1, abort, status))) break;
-        if (!(ok = mbar_wait(smem_u32(&sm.kv_full[nb_]), ((it + 1) >> 1) & 1, abort, status))) break;
+        if (!(ok = mbar_wait(smem_u32(&sm.v_full[t % kDqVStages]), (t / kDqVStages) & 1, abort, status))) break;
         tc_fence_after();
-        issue_dp(nb_);
-        if (it >= 1 && !(ok = mbar_wait(smem_u32(&sm.dq_done[nb_]), ((it - 1) >> 1) & 1, abort, status))) break;
+        issue_dp(t);
+        if (!(ok = mbar_wait(smem_u32(&sm.k_full[t % kDqKStages]), (t / kDqKStages) & 1, abort, status))) break;
+        if (it >= 1 && !(ok = mbar_wait(smem_u32(&sm.dq_done[t & 1]), ((it - 1) >> 1) & 1, abort, status))) break;
         tc_fence_after();
-        issue_s(nb_, nb_);
+        issue_s(t);
       }
       tc_commit(smem_u32(&sm.in_done));
       drain_wait(smem_u32(&sm.in_done), 0);
@@ -223,8 +244,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const uint64_t dkmn0 = smem_desc(smem_u32(sm.k[0]), kHalf, 1024, kSwizzle128B);
       bool ok = true;
       for (int it = 0; ok && it < cnt; ++it) {
-        const int b = it & 1, st = it & 1;
-        const uint64_t dkt = desc_at(dkmn0, st * kTile);
+        const int b = it & 1, ks = it % kDqKStages;
+        const uint64_t dkt = desc_at(dkmn0, ks * kTile);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           if (!(ok = mbar_wait(smem_u32(&sm.ds_full[b][half]), (it >> 1) & 1, abort, status))) break;
@@ -235,7 +256,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                    (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        tc_commit(smem_u32(&sm.kv_empty[st]));
+        tc_commit(smem_u32(&sm.k_empty[ks]));
         tc_commit(smem_u32(&sm.dq_done[b]));
       }
       // every dQ product has completed once this barrier flips; every S and dP product
