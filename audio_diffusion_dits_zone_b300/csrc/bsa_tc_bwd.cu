@@ -91,6 +91,7 @@ struct DqSmem {
   uint64_t s_full[2], dp_full, dp_free;
   uint64_t ds_full[2][2];  // [S buffer][key half]
   uint64_t dq_done[2];     // dQ(t) has read S buffer t & 1
+  uint64_t a_issued;       // the S / dP issuer has enqueued block t + 1's products
   uint64_t acc_done, in_done;
   uint32_t tmem_base;
   int abort;
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(smem_u32(&sm.dp_free), 8);
     mbar_init(smem_u32(&sm.dq_done[0]), 1);
     mbar_init(smem_u32(&sm.dq_done[1]), 1);
+    mbar_init(smem_u32(&sm.a_issued), 1);
     mbar_init(smem_u32(&sm.acc_done), 1);
     mbar_init(smem_u32(&sm.in_done), 1);
     sm.abort = 0;
@@ -233,6 +235,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (it >= 1 && !(ok = mbar_wait(smem_u32(&sm.dq_done[t & 1]), ((it - 1) >> 1) & 1, abort, status))) break;
         tc_fence_after();
         issue_s(t);
+        mbar_arrive(smem_u32(&sm.a_issued));  // dQ(t - 1) may follow them into the tensor pipe
       }
       tc_commit(smem_u32(&sm.in_done));
       drain_wait(smem_u32(&sm.in_done), 0);
@@ -246,6 +249,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       for (int it = 0; ok && it < cnt; ++it) {
         const int b = it & 1, ks = it % kDqKStages;
         const uint64_t dkt = desc_at(dkmn0, ks * kTile);
+        // the next block's S and dP go first: the softmax waits on them, nothing waits on dQ
+        if (it + 1 < cnt && !(ok = mbar_wait(smem_u32(&sm.a_issued), it & 1, abort, status))) break;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           if (!(ok = mbar_wait(smem_u32(&sm.ds_full[b][half]), (it >> 1) & 1, abort, status))) break;
