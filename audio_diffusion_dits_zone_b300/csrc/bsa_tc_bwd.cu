@@ -278,6 +278,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int row = i * kB + r;
     const float l2 = L2[(size_t)h * npad + row];
     const float dr = Dp[(size_t)h * npad + row];
+    const f2 scale2 = f2_make(kSl2, kSl2), neg_l2 = f2_make(-l2, -l2), neg_dr = f2_make(-dr, -dr);
     bool ok = true;
     int j_next = cnt > 0 ? lst[0] : 0;  // block indices are read one block ahead
     for (int it = 0; it < cnt; ++it) {
@@ -317,9 +318,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * x]), kSl2, -l2));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * x + 1]), kSl2, -l2));
-          pk[x] = pack_bf16x2(p0 * (__uint_as_float(pr[2 * x]) - dr), p1 * (__uint_as_float(pr[2 * x + 1]) - dr));
+          float a0, a1;
+          f2_split(f2_fma(f2_make(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), scale2, neg_l2), a0, a1);
+          const f2 p = f2_make(fast_exp2(a0), fast_exp2(a1));
+          const f2 g = f2_add(f2_make(__uint_as_float(pr[2 * x]), __uint_as_float(pr[2 * x + 1])), neg_dr);
+          pk[x] = f2_pack_bf16(f2_mul(p, g));  // dS = P (dP - D)
         }
         tmem_st16(lane_base + b * 128 + c0 + cc * 16, pk);
       }
@@ -539,6 +542,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const int c = quarter * 32 + lane;  // key row of block j = TMEM lane
     const int q0 = half * 64;           // this thread's query columns q0 .. q0 + 63
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const f2 scale2 = f2_make(kSl2, kSl2);
     bool ok = true;
     for (int it = 0; it < cnt; ++it) {
       const int s = it & 1;
@@ -561,15 +565,17 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         for (int q4 = 0; q4 < 8; ++q4) {  // 4 query columns per vector load of the row statistics
           const float4 L = l2v[cc * 8 + q4];
           const float4 Dv = drv[cc * 8 + q4];
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4]), kSl2, -L.x));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 1]), kSl2, -L.y));
-          const float p2 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 2]), kSl2, -L.z));
-          const float p3 = fast_exp2(fmaf(__uint_as_float(sr[4 * q4 + 3]), kSl2, -L.w));
-          pp[2 * q4] = pack_bf16x2(p0, p1);
-          pp[2 * q4 + 1] = pack_bf16x2(p2, p3);
-          dd[2 * q4] = pack_bf16x2(p0 * (__uint_as_float(pr[4 * q4]) - Dv.x), p1 * (__uint_as_float(pr[4 * q4 + 1]) - Dv.y));
-          dd[2 * q4 + 1] =
-              pack_bf16x2(p2 * (__uint_as_float(pr[4 * q4 + 2]) - Dv.z), p3 * (__uint_as_float(pr[4 * q4 + 3]) - Dv.w));
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {  // two query columns per packed pair
+            const int e = 4 * q4 + 2 * u;
+            const f2 nl = u ? f2_make(-L.z, -L.w) : f2_make(-L.x, -L.y);
+            const f2 nd = u ? f2_make(-Dv.z, -Dv.w) : f2_make(-Dv.x, -Dv.y);
+            float a0, a1;
+            f2_split(f2_fma(f2_make(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), scale2, nl), a0, a1);
+            const f2 p = f2_make(fast_exp2(a0), fast_exp2(a1));
+            pp[2 * q4 + u] = f2_pack_bf16(p);
+            dd[2 * q4 + u] = f2_pack_bf16(f2_mul(p, f2_add(f2_make(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])), nd)));
+          }
         }
         // P^T_x over the first 32 columns of S^T_x, dS^T_x over the first 32 of dP^T_x
         // (this chunk's columns were read above; the writes land in columns already read)

@@ -320,13 +320,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = c < len ? s[c] : -INFINITY;
       }
+      // row max: eight chains of three-input maxima
       float m8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) m8[k] = s[k];
 #pragma unroll
-      for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      for (int c = 8; c < 128; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = max3(m8[k], s[c + k], s[c + 8 + k]);
+      const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       const float m_new = fmaxf(m_used, mx * kSl2);
       if (m_new > m_used + kRescaleLog2) {
         const float alpha = fast_exp2(m_used - m_new);
@@ -350,21 +352,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // no live key yet (only skipped blocks so far): P = 0 (warp-uniform)
       const float neg_m = m_used > -INFINITY ? -m_used : -INFINITY;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      const f2 scale2 = f2_make(kSl2, kSl2), shift2 = f2_make(neg_m, neg_m);
+      f2 ls2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int x = 0; x < 32; ++x) {
           const int c = half * 64 + 2 * x;
-          const float p0 = fast_exp2(fmaf(s[c], kSl2, neg_m));
-          const float p1 = fast_exp2(fmaf(s[c + 1], kSl2, neg_m));
-          ls[x & 3] += p0 + p1;
+          float a0, a1;
+          f2_split(f2_fma(f2_make(s[c], s[c + 1]), scale2, shift2), a0, a1);  // s * log2(e)/sqrt(d) - m
+          const float p0 = fast_exp2(a0);
+          const float p1 = fast_exp2(a1);
+          ls2[x & 1] = f2_add(ls2[x & 1], f2_make(p0, p1));
           pk[x] = pack_bf16x2(p0, p1);
         }
         tmem_st32(lane_base + b * 128 + half * 32, pk);
       }
-      const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      float l0, l1, l2_, l3;
+      f2_split(ls2[0], l0, l1);
+      f2_split(ls2[1], l2_, l3);
+      const float lsum = (l0 + l1) + (l2_ + l3);
       tmem_wait_st();
       l += lsum;
       tc_fence_before();
