@@ -34,7 +34,6 @@ constexpr int kB = 128;
 constexpr int kD = 128;
 constexpr uint32_t kHalf = 16384;
 constexpr uint32_t kTile = 2 * kHalf;
-constexpr int kThreads = 192;  // warps: 0 producer, 1 MMA, 2-5 rows
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSl2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
 constexpr float kScale = 0.08838834764831845f;                      // 1 / sqrt(128)

@@ -211,7 +211,7 @@ def run_ours(args, rank, world, local_rank):
     algo = {
         "bsa_fwd_tc": ("tensor", 4.0 * pairs * wl.d), "bsa_dq_tc": ("tensor", 6.0 * pairs * wl.d),
         "bsa_dkdv_tc": ("tensor", 8.0 * pairs * wl.d),
-        "zone_partial": ("hbm", wl.N * C * 2.0),
+        "zone_tma": ("hbm", wl.N * C * 2.0), "zone_partial": ("hbm", wl.N * C * 2.0),
         "pool_gather": ("hbm", 6.0 * wl.N * C * 2 + 2.0 * wl.heads * wl.nb * wl.d * 4),
         "scores": ("hbm", wl.heads * wl.nb ** 2 * 4.0 + 2.0 * wl.heads * wl.nb * wl.d * 4),
         "select": ("hbm", wl.heads * wl.nb ** 2 * 4.0 + wl.heads * wl.nb * 4 + 4.0 * kept),
