@@ -382,9 +382,9 @@ struct DkdvSmem {
   float dr[2][kB];  // D of the stage's query rows
   uint64_t kv_full;
   uint64_t qdo_full[2], qdo_empty[2];
-  uint64_t sdp_full[2];  // [query half]: S^T and dP^T of that half computed
-  uint64_t pds_full[2];  // [query half]: P^T and dS^T of that half written
-  uint64_t vk_done[2];   // [query half]: dV and dK have read that half's P^T and dS^T
+  uint64_t s_full[2], dp_full[2];  // [query half]: S^T, dP^T of that half computed
+  uint64_t p_full[2], ds_full[2];  // [query half]: P^T, dS^T of that half written
+  uint64_t v_done[2], k_done[2];   // [query half]: dV has read P^T / dK has read dS^T
   uint64_t acc_done, in_done;
   uint32_t tmem_base;
   int abort;
@@ -398,10 +398,11 @@ static_assert(sizeof(QdoStage) % 1024 == 0, "stages keep 1024-byte alignment for
 // Per query half x and pair t:  S^T_x = K Q_x^T and dP^T_x = V dO_x^T (N = 64);
 // the half's warpgroup writes P^T_x (bf16) over the first 32 columns of S^T_x and
 // dS^T_x over the first 32 of dP^T_x; dV += P^T_x dO_x and dK += dS^T_x Q_x (K = 64).
-// Two issuing threads: warp 10 issues dV/dK of a half as soon as it is written;
-// warp 1 issues the next pair's S^T_x, dP^T_x once those dV/dK products have
-// completed.  The halves alternate in the tensor pipe, so one half's products run
-// while the other half's softmax gradient is computed.
+// Two issuing threads: warp 10 issues dV of a half as soon as its P^T is written and
+// dK as soon as its dS^T is; warp 1 issues the next pair's S^T_x once that dV has
+// completed and dP^T_x once that dK has.  So a half's S^T -> P^T -> dV chain does not
+// wait for its dS^T, and the halves alternate in the tensor pipe: one half's products
+// run while the other half's softmax gradient is computed.
 __global__ void __launch_bounds__(kDkdvThreads, 1)
     bsa_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -421,9 +422,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sm.qdo_full[s]), 1);
       mbar_init(smem_u32(&sm.qdo_empty[s]), 1);
-      mbar_init(smem_u32(&sm.sdp_full[s]), 1);
-      mbar_init(smem_u32(&sm.pds_full[s]), 4);
-      mbar_init(smem_u32(&sm.vk_done[s]), 1);
+      mbar_init(smem_u32(&sm.s_full[s]), 1);
+      mbar_init(smem_u32(&sm.dp_full[s]), 1);
+      mbar_init(smem_u32(&sm.p_full[s]), 4);
+      mbar_init(smem_u32(&sm.ds_full[s]), 4);
+      mbar_init(smem_u32(&sm.v_done[s]), 1);
+      mbar_init(smem_u32(&sm.k_done[s]), 1);
     }
     mbar_init(smem_u32(&sm.acc_done), 1);
     mbar_init(smem_u32(&sm.in_done), 1);
@@ -488,15 +492,20 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         for (int half = 0; half < 2; ++half) {
           // the half's rows of the Q / dO tiles start 64 rows (8 KB) into each box
           const uint64_t dq = desc_at(dq0, so + half * 8192), ddo = desc_at(ddo0, so + half * 8192);
-          if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.vk_done[half]), (it - 1) & 1, abort, status))) break;
+          // S^T_x overwrites the P^T_x that the previous pair's dV read
+          if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.v_done[half]), (it - 1) & 1, abort, status))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + half * 64, desc_at(dk_k, koff(kk)), desc_at(dq, koff(kk)), id_h, kk > 0);
+          tc_commit(smem_u32(&sm.s_full[half]));
+          // dP^T_x overwrites the dS^T_x that the previous pair's dK read
+          if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.k_done[half]), (it - 1) & 1, abort, status))) break;
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + 128 + half * 64, desc_at(dk_v, koff(kk)), desc_at(ddo, koff(kk)), id_h, kk > 0);
-          tc_commit(smem_u32(&sm.sdp_full[half]));
+          tc_commit(smem_u32(&sm.dp_full[half]));
         }
       }
       tc_commit(smem_u32(&sm.in_done));
@@ -515,17 +524,20 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         const uint64_t dqmn = desc_at(dqmn0, so), ddomn = desc_at(ddomn0, so);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          if (!(ok = mbar_wait(smem_u32(&sm.pds_full[half]), it & 1, abort, status))) break;
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[half]), it & 1, abort, status))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // dV += P^T_x dO_x
             mma_ts(tmem + 256, tmem + half * 64 + kk * 8, desc_at(ddomn, (half * 4 + kk) * 2048), id_ts,
                    (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&sm.v_done[half]));
+          if (!(ok = mbar_wait(smem_u32(&sm.ds_full[half]), it & 1, abort, status))) break;
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // dK += dS^T_x Q_x
             mma_ts(tmem + 384, tmem + 128 + half * 64 + kk * 8, desc_at(dqmn, (half * 4 + kk) * 2048), id_ts,
                    (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(smem_u32(&sm.vk_done[half]));
+          tc_commit(smem_u32(&sm.k_done[half]));
         }
         if (!ok) break;
         tc_commit(smem_u32(&sm.qdo_empty[s]));
@@ -546,45 +558,64 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     for (int it = 0; it < cnt; ++it) {
       const int s = it & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status) &&
-                                       mbar_wait(smem_u32(&sm.sdp_full[half]), it & 1, abort, status));
+                                       mbar_wait(smem_u32(&sm.s_full[half]), it & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
       const float4* l2v = reinterpret_cast<const float4*>(sm.l2[s] + q0);
       const float4* drv = reinterpret_cast<const float4*>(sm.dr[s] + q0);
+      f2 p[32];  // P^T of this key row and the half's 64 query columns, fp32 pairs
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {  // 32 query columns at a time
-        uint32_t sr[32], pr[32];
-        tmem_ld32(lane_base + q0 + cc * 32, sr);
-        tmem_ld32(lane_base + 128 + q0 + cc * 32, pr);
-        tmem_wait_ld();
-        reg_fence(sr);
-        reg_fence(pr);
-        uint32_t pp[16], dd[16];
+        uint32_t sr[32];
+        tmem_load_row32(lane_base + q0 + cc * 32, sr);
+        uint32_t pp[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {  // 4 query columns per vector load of the row statistics
           const float4 L = l2v[cc * 8 + q4];
-          const float4 Dv = drv[cc * 8 + q4];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {  // two query columns per packed pair
             const int e = 4 * q4 + 2 * u;
             const f2 nl = u ? f2_make(-L.z, -L.w) : f2_make(-L.x, -L.y);
-            const f2 nd = u ? f2_make(-Dv.z, -Dv.w) : f2_make(-Dv.x, -Dv.y);
             float a0, a1;
             f2_split(f2_fma(f2_make(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), scale2, nl), a0, a1);
-            const f2 p = f2_make(fast_exp2(a0), fast_exp2(a1));
-            pp[2 * q4 + u] = f2_pack_bf16(p);
-            dd[2 * q4 + u] = f2_pack_bf16(f2_mul(p, f2_add(f2_make(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])), nd)));
+            p[cc * 16 + 2 * q4 + u] = f2_make(fast_exp2(a0), fast_exp2(a1));
+            pp[2 * q4 + u] = f2_pack_bf16(p[cc * 16 + 2 * q4 + u]);
           }
         }
-        // P^T_x over the first 32 columns of S^T_x, dS^T_x over the first 32 of dP^T_x
-        // (this chunk's columns were read above; the writes land in columns already read)
+        // P^T_x over the first 32 columns of S^T_x (this chunk's columns were read above;
+        // the writes land in columns already read)
         tmem_st16(lane_base + q0 + cc * 16, pp);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[half]));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dp_full[half]), it & 1, abort, status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t pr[32];
+        tmem_load_row32(lane_base + 128 + q0 + cc * 32, pr);
+        uint32_t dd[16];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 Dv = drv[cc * 8 + q4];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int e = 4 * q4 + 2 * u;
+            const f2 nd = u ? f2_make(-Dv.z, -Dv.w) : f2_make(-Dv.x, -Dv.y);
+            dd[2 * q4 + u] = f2_pack_bf16(
+                f2_mul(p[cc * 16 + 2 * q4 + u], f2_add(f2_make(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])), nd)));
+          }
+        }
+        // dS^T_x over the first 32 columns of dP^T_x
         tmem_st16(lane_base + 128 + q0 + cc * 16, dd);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.pds_full[half]));
+      if (lane == 0) mbar_arrive(smem_u32(&sm.ds_full[half]));
     }
     const int col = j * kB + c;
     __nv_bfloat16* dk_row = dk + (int64_t)col * ld + (int64_t)h * kD + q0;

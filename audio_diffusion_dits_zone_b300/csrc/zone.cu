@@ -15,12 +15,12 @@
 // clipped at the zone edge, tokens raster inside a tile.
 //
 // Kernels (all HBM-bound or tiny):
-//   zone_tma       (bf16 features, zones up to 3 x 9 x 16) persistent CTAs of 4 warps;
-//                  each warp streams its own (zone, 64-channel) items as two 32-channel
-//                  slabs: one 4D TMA box [t][h][w][32 channels] per slab into a
+//   zone_tma       (bf16 features, zones up to 3 x 9 in t x h) persistent CTAs of 8
+//                  warps; each warp streams its own (zone, 64-channel) items as slabs of
+//                  4 w columns: one 4D TMA box [t][h][w][64 channels] per slab into a
 //                  double-buffered shared-memory stage, so the next slab is in flight
-//                  while this one is reduced (lane = channel, all line sums in
-//                  registers, same arithmetic as zone_lines);
+//                  while this one is reduced (lane = 2 channels on packed fp32 pairs, all
+//                  line sums in registers, same arithmetic as zone_lines);
 //   zone_lines     (zones up to 3 x 9 or 5 x 8 in t x h, even channel counts) one warp
 //                  per (zone, 64 channels), lane = 2 channels, so every load is one
 //                  128-byte run of a token row.  The warp streams the zone once,
@@ -284,43 +284,86 @@ __global__ void __launch_bounds__(kLinesWarps * 32) zone_lines_kernel(const T* _
   if (lane < 3) part[((size_t)z * nchunks + chunk) * 3 + lane] = lane == 0 ? ss[0] : (lane == 1 ? ss[1] : ss[2]);
 }
 
-constexpr int kTmaWarps = 4;
-constexpr int kSlabCh = 32;                        // channels per slab (64 bytes per token)
-constexpr int kSlabMaxBytes = 3 * 9 * 16 * kSlabCh * 2;  // one 3 x 9 x 16 zone box
-constexpr int kTmaStages = 2;                      // per warp
+constexpr int kTmaWarps = 8;
+constexpr int kSlabCh = 64;     // channels per slab: one 128-byte run of each token row, two per lane
+constexpr int kWq = 4;          // w columns per slab (a quarter of a 16-wide zone)
+constexpr int kTmaStages = 2;   // per warp
+constexpr int kTmaMT = 3, kTmaMH = 9;  // slab extent along t and h (zones up to 3 x 9 in t x h)
+constexpr int kSlabBytes = kTmaMT * kTmaMH * kWq * kSlabCh * 2;  // 13,824 bytes
 
 struct ZoneTmaSmem {
-  uint8_t slab[kTmaWarps][kTmaStages][kSlabMaxBytes];
+  uint8_t slab[kTmaWarps][kTmaStages][kSlabBytes];
   uint64_t full[kTmaWarps][kTmaStages];
 };
 
+// One slab [MT][MH][kWq][64 channels] bf16 of one (zone, 64 channels) item: accumulate,
+// for this lane's channel pair, the shifted values v = x - x0 into the line sums along
+// t (squared into bt per (h, w)), along h (squared into bh per (t, w)), along w (kept in
+// wsum[t][h] across the item's slabs) and their squares (sq, one chain per t).
+// CLIP: positions outside the zone (t >= Lt, h >= Lh, column >= wlim) count as 0.
+template <int MT, int MH, bool CLIP>
+__device__ __forceinline__ void zone_slab_sums(const uint8_t* slab, int lane, f2 nx0, int Lt, int Lh, int wlim,
+                                               f2 (&wsum)[MT][MH], f2 (&sq)[MT], f2& bt, f2& bh) {
+  const uint32_t* base = reinterpret_cast<const uint32_t*>(slab) + lane;
+  const f2 zero{0ull};
+#pragma unroll 1
+  for (int w = 0; w < kWq; ++w) {
+    f2 hs[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) hs[t] = zero;
+#pragma unroll
+    for (int h = 0; h < MH; ++h) {
+      f2 ts = zero;
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const uint32_t raw = base[((t * MH + h) * kWq + w) * (kSlabCh / 2)];
+        f2 v = f2_add(f2_make(__uint_as_float(raw << 16), __uint_as_float(raw & 0xffff0000u)), nx0);
+        if (CLIP && !(t < Lt && h < Lh && w < wlim)) v = zero;
+        ts = f2_add(ts, v);
+        hs[t] = f2_add(hs[t], v);
+        wsum[t][h] = f2_add(wsum[t][h], v);
+        sq[t] = f2_fma(v, v, sq[t]);
+      }
+      bt = f2_fma(ts, ts, bt);
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) bh = f2_fma(hs[t], hs[t], bh);
+  }
+}
+
 // part[(z * nchunks + chunk) * 3 + a] exactly as zone_lines_kernel (chunk = 64 channels),
-// from slabs loaded with the 4D tensor map tm = feature viewed as [T][H][W][C] bf16.
+// from slabs loaded with the 4D tensor map tm = feature viewed as [T][H][W][C] bf16 with
+// box {64, kWq, MH, MT}.  Persistent CTAs of kTmaWarps warps; each warp streams its own
+// items, nq slabs (w quarters) per item, through a two-stage ring that its lane 0 refills
+// (so the next slab is in flight while this one is reduced).  Zones that fill the box
+// take the unpredicated path; zones clipped by the grid (or smaller than the box) mask
+// the positions outside them, whose slab bytes are zero fill or a neighbour's tokens.
 template <int MT, int MH>
 __global__ void __launch_bounds__(kTmaWarps * 32, 1)
-    zone_tma_kernel(const __grid_constant__ CUtensorMap tm, ZoneGeom g, int nchunks, int items,
+    zone_tma_kernel(const __grid_constant__ CUtensorMap tm, ZoneGeom g, int nchunks, int items, int nq,
                     float* __restrict__ part, uint32_t* status) {
+  static_assert(MT * MH * kWq * kSlabCh * 2 <= kSlabBytes, "slab larger than its stage");
   extern __shared__ uint8_t smem_raw[];
   ZoneTmaSmem& sm = *reinterpret_cast<ZoneTmaSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slab_bytes = g.zt * g.zh * g.zw * kSlabCh * 2;
   if (lane == 0) {
     for (int s = 0; s < kTmaStages; ++s) mbar_init(smem_u32(&sm.full[warp][s]), 1);
     mbar_fence_init();
   }
   __syncwarp();
-  // this warp's items: k = (blockIdx.x * kTmaWarps + warp) + n * stride, two slabs each
+  // this warp's items: k = (blockIdx.x * kTmaWarps + warp) + n * stride, nq slabs each
   const int stride = gridDim.x * kTmaWarps;
   const int first = blockIdx.x * kTmaWarps + warp;
   const int nmine = first < items ? (items - first + stride - 1) / stride : 0;
-  const int nslabs = 2 * nmine;
+  const int nslabs = nq * nmine;
   auto issue = [&](int s) {  // slab s of this warp -> stage s & 1
-    const int k = first + (s >> 1) * stride;
+    const int n = s / nq, q = s - n * nq;
+    const int k = first + n * stride;
     const int z = k / nchunks, chunk = k - z * nchunks;
     const ZoneBox b = zone_box(g, z);
     const uint32_t bar = smem_u32(&sm.full[warp][s & 1]);
-    mbar_arrive_expect_tx(bar, (uint32_t)slab_bytes);
-    tma_load_4d(smem_u32(sm.slab[warp][s & 1]), &tm, chunk * 64 + (s & 1) * kSlabCh, b.w0, b.h0, b.t0, bar);
+    mbar_arrive_expect_tx(bar, (uint32_t)(MT * MH * kWq * kSlabCh * 2));
+    tma_load_4d(smem_u32(sm.slab[warp][s & 1]), &tm, chunk * kSlabCh, b.w0 + q * kWq, b.h0, b.t0, bar);
   };
   int issued = 0;  // lane 0: slabs issued so far
   if (lane == 0) {
@@ -328,65 +371,62 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1)
     for (int s = 0; s < kTmaStages && s < nslabs; ++s) issue(s), ++issued;
   }
   int abort = 0;
-  float ss[3] = {0.f, 0.f, 0.f};
+  const f2 zero{0ull};
+  f2 wsum[MT][MH], sq[MT], bt = zero, bh = zero, nx0 = zero;
   for (int s = 0; s < nslabs; ++s) {
-    const int k = first + (s >> 1) * stride;
+    const int n = s / nq, q = s - n * nq;
+    const int k = first + n * stride;
     const int z = k / nchunks, chunk = k - z * nchunks;
     const ZoneBox b = zone_box(g, z);
     const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[warp][s & 1]), (s >> 1) & 1, &abort, status));
     if (!ok) break;
-    // slab layout [t][h][w][32 channels] bf16 with the full box extents (zt, zh, zw);
-    // positions past a clipped zone's edge hold zeros and are skipped
-    const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(sm.slab[warp][s & 1]) + lane;
-    const int sw = kSlabCh, shh = g.zw * kSlabCh, stt = g.zh * g.zw * kSlabCh;
-    const float x0 = __bfloat162float(xs[0]);
-    float wsum[MT][MH];
+    const uint8_t* slab = sm.slab[warp][s & 1];
+    if (q == 0) {  // new item: reset the sums; shift by the zone's first token
 #pragma unroll
-    for (int t = 0; t < MT; ++t)
+      for (int t = 0; t < MT; ++t) {
+        sq[t] = zero;
 #pragma unroll
-      for (int h = 0; h < MH; ++h) wsum[t][h] = 0.f;
-    float sq = 0.f, bt = 0.f, bh = 0.f;
-    for (int w = 0; w < b.Lw; ++w) {
-      float hs[MT];
-#pragma unroll
-      for (int t = 0; t < MT; ++t) hs[t] = 0.f;
-#pragma unroll
-      for (int h = 0; h < MH; ++h) {
-        float ts = 0.f;
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          const bool in = h < b.Lh && t < b.Lt;
-          const float v = in ? __bfloat162float(xs[t * stt + h * shh + w * sw]) - x0 : 0.f;
-          ts += v;
-          hs[t] += v;
-          wsum[t][h] += v;
-          sq = fmaf(v, v, sq);
-        }
-        bt = fmaf(ts, ts, bt);
+        for (int h = 0; h < MH; ++h) wsum[t][h] = zero;
       }
-#pragma unroll
-      for (int t = 0; t < MT; ++t) bh = fmaf(hs[t], hs[t], bh);
+      bt = bh = zero;
+      const uint32_t raw = reinterpret_cast<const uint32_t*>(slab)[lane];
+      nx0 = f2_make(-__uint_as_float(raw << 16), -__uint_as_float(raw & 0xffff0000u));
     }
+    const int wlim = b.Lw - q * kWq;  // columns of this slab inside the zone
+    if (b.Lt == MT && b.Lh == MH && wlim >= kWq)
+      zone_slab_sums<MT, MH, false>(slab, lane, nx0, MT, MH, kWq, wsum, sq, bt, bh);
+    else
+      zone_slab_sums<MT, MH, true>(slab, lane, nx0, b.Lt, b.Lh, wlim, wsum, sq, bt, bh);
     // every lane has read the stage: refill it with slab s + 2
     __syncwarp();
     if (lane == 0 && s + kTmaStages < nslabs) issue(s + kTmaStages), ++issued;
-    float bw = 0.f;
+    if (q == nq - 1) {  // the item's last slab: one partial per (zone, 64 channels)
+      f2 bw = zero;
 #pragma unroll
-    for (int t = 0; t < MT; ++t)
+      for (int t = 0; t < MT; ++t)
 #pragma unroll
-      for (int h = 0; h < MH; ++h) bw = fmaf(wsum[t][h], wsum[t][h], bw);
-    const float bl[3] = {bt, bh, bw};
-    const int L[3] = {b.Lt, b.Lh, b.Lw};
+        for (int h = 0; h < MH; ++h) bw = f2_fma(wsum[t][h], wsum[t][h], bw);
+      f2 sqa = sq[0];
 #pragma unroll
-    for (int a = 0; a < 3; ++a)
-      if (L[a] > 1) ss[a] += fmaxf(sq - bl[a] / (float)L[a], 0.f);
-    if (s & 1) {  // both halves of the item done: one partial per (zone, 64 channels)
+      for (int t = 1; t < MT; ++t) sqa = f2_add(sqa, sq[t]);
+      float sqv[2], bl[3][2];
+      f2_split(sqa, sqv[0], sqv[1]);
+      f2_split(bt, bl[0][0], bl[0][1]);
+      f2_split(bh, bl[1][0], bl[1][1]);
+      f2_split(bw, bl[2][0], bl[2][1]);
+      const int L[3] = {b.Lt, b.Lh, b.Lw};
+      float ss[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+      for (int a = 0; a < 3; ++a)
+        if (L[a] > 1) {
+          const float inv = 1.f / (float)L[a];
+          ss[a] = fmaxf(sqv[0] - bl[a][0] * inv, 0.f) + fmaxf(sqv[1] - bl[a][1] * inv, 0.f);
+        }
 #pragma unroll
       for (int a = 0; a < 3; ++a)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss[a] += __shfl_xor_sync(0xffffffffu, ss[a], o);
       if (lane < 3) part[((size_t)z * nchunks + chunk) * 3 + lane] = lane == 0 ? ss[0] : (lane == 1 ? ss[1] : ss[2]);
-      ss[0] = ss[1] = ss[2] = 0.f;
     }
   }
   // a warp that gave up waits (bounded) for the copies it still has in flight: the
@@ -525,8 +565,9 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // The TMA kernel applies: bf16, 16-byte aligned rows (ld % 8 == 0), whole 64-channel
 // chunks, zones of at most 3 x 9 x 16 tokens.
 bool tma_variant(const ZoneGeom& g, int C, int64_t ld, int dtype, const void* feat) {
-  return dtype == PRISM_BF16 && C % 64 == 0 && ld % 8 == 0 && (reinterpret_cast<uintptr_t>(feat) & 15) == 0 &&
-         std::min(g.zt, g.T) <= 3 && std::min(g.zh, g.H) <= 9 && std::min(g.zw, g.W) <= 16;
+  // the box spans kTmaMT x kTmaMH (t, h) tokens, so the grid must be at least that large
+  return dtype == PRISM_BF16 && C % kSlabCh == 0 && ld % 8 == 0 && (reinterpret_cast<uintptr_t>(feat) & 15) == 0 &&
+         g.T >= kTmaMT && g.H >= kTmaMH && g.W >= kWq && std::min(g.zt, g.T) <= kTmaMT && std::min(g.zh, g.H) <= kTmaMH;
 }
 
 int lines_variant(const ZoneGeom& g, int C, int64_t ld, int dtype, const void* feat) {
@@ -560,16 +601,15 @@ cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const fl
   const dim3 grid(g.Z, nchunks);
   cudaError_t e;
   if (tma_variant(g, C, ld, dtype, feat)) {
-    // feature as [T][H][W][C] bf16; the box is one zone (clipped zones read zeros past the grid)
+    // feature as [T][H][W][C] bf16; one box = 64 channels of kWq columns of a zone's
+    // MT x MH (t, h) extent (clipped zones read zeros past the grid)
     CUtensorMap tm;
     const uint64_t dims[4] = {(uint64_t)C, (uint64_t)g.W, (uint64_t)g.H, (uint64_t)g.T};
     const uint64_t strides[3] = {(uint64_t)ld * 2, (uint64_t)g.W * ld * 2, (uint64_t)g.H * g.W * ld * 2};
-    const uint32_t box[4] = {(uint32_t)kSlabCh, (uint32_t)std::min(g.zw, g.W), (uint32_t)std::min(g.zh, g.H),
-                             (uint32_t)std::min(g.zt, g.T)};
-    ZoneGeom gb = g;  // slab layout uses the box extents
-    gb.zt = (int)box[3], gb.zh = (int)box[2], gb.zw = (int)box[1];
+    const uint32_t box[4] = {(uint32_t)kSlabCh, (uint32_t)kWq, (uint32_t)kTmaMH, (uint32_t)kTmaMT};
     if (!tensor_map_bf16(&tm, feat, 4, dims, strides, box)) return cudaErrorInvalidValue;
     const int items = g.Z * nchunks;
+    const int nq = (std::min(g.zw, g.W) + kWq - 1) / kWq;
     int sms = 148;
     {
       int dev = 0;
@@ -577,11 +617,11 @@ cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const fl
     }
     const int grid = std::max(1, std::min(sms, (items + kTmaWarps - 1) / kTmaWarps));
     const size_t smem_t = sizeof(ZoneTmaSmem) + 128;
-    if ((e = cudaFuncSetAttribute(zone_tma_kernel<3, 9>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t)) !=
-        cudaSuccess)
+    auto kern = zone_tma_kernel<kTmaMT, kTmaMH>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t)) != cudaSuccess)
       return e;
     HookScope hs("zone_tma", st);
-    zone_tma_kernel<3, 9><<<grid, kTmaWarps * 32, smem_t, st>>>(tm, gb, nchunks, items, part, status);
+    kern<<<grid, kTmaWarps * 32, smem_t, st>>>(tm, g, nchunks, items, nq, part, status);
   } else if (variant) {
     const dim3 lgrid((nchunks + kLinesWarps - 1) / kLinesWarps, g.Z);
     HookScope hs("zone_lines", st);
