@@ -22,6 +22,13 @@ Input recipe (the pages fix none of it; these are the readings used here):
   * A2V cross-attention feature-norm field: a sum of unit-amplitude isotropic 3D
     Gaussian bumps over token coordinates, centres uniform over the grid.
   * dO ~ N(0, 1) per (head), in block order (it is i.i.d., so the order is moot).
+  * Audio-to-video cross-attention (the step that produces the A2V field): video
+    queries drawn like V (sinusoids over (t,h,w) + noise, no rotary embedding, since
+    audio and video share no position frame); audio keys and values per head the
+    same way over the 1D audio time axis (6 sinusoids of frequency U[0, 0.25)
+    cycles/token + noise).  AUDIO_TOKENS = 157 audio tokens: the 81 video frames at
+    16 fps span 5.06 s, taken at 31 audio latent frames per second (a reading; the
+    pages give no audio token rate).
   * Seeds: numpy PCG64 from SeedSequence([0, config id, tensor id, head]).
 
 Values are generated in float32; ``to_bf16`` rounds them to bfloat16 (round to
@@ -38,6 +45,8 @@ import numpy as np
 
 Q_ID, K_ID, V_ID, DO_ID = 0, 1, 2, 3
 A2V_ID = 100
+AQ_ID, AK_ID, AV_ID = 10, 11, 12  # video queries, audio keys, audio values of the cross-attention
+AUDIO_TOKENS = 157
 
 
 @dataclass(frozen=True)
@@ -151,6 +160,30 @@ def gen_head(wl: Workload, tensor: int, head: int, rope=None) -> np.ndarray:
         cos, sin = rope if rope is not None else rope_tables(wl.grid, wl.d, wl.rope_split)
         x = _apply_rope(x, cos, sin)
     return x
+
+
+def gen_audio_head(wl: Workload, tensor: int, head: int, M: int = AUDIO_TOKENS) -> np.ndarray:
+    """One head of the audio keys (AK_ID) or values (AV_ID): float32 [M, d] over the
+    audio time axis."""
+    rng = _rng(wl.cid, tensor, head)
+    f = rng.uniform(0.0, 0.25, size=6)
+    phi = rng.uniform(0.0, 2.0 * math.pi, size=6)
+    a = rng.normal(0.0, math.sqrt(1.0 / 6.0), size=(6, wl.d))
+    tau = np.arange(M, dtype=np.float64)[:, None]
+    waves = np.sin(2.0 * math.pi * f[None, :] * tau + phi[None, :])
+    x = (waves @ a).astype(np.float32)
+    x += rng.standard_normal((M, wl.d), dtype=np.float32) * np.float32(0.1)
+    return x
+
+
+def gen_a2v_inputs(wl: Workload, heads, M: int = AUDIO_TOKENS):
+    """Video queries [N, Hh, d] and audio keys / values [M, Hh, d] of the cross-attention,
+    rounded like every other input of the workload."""
+    heads = list(heads)
+    qv = np.stack([round_inputs(wl, gen_head(wl, AQ_ID, h)) for h in heads], axis=1)
+    ka = np.stack([round_inputs(wl, gen_audio_head(wl, AK_ID, h, M)) for h in heads], axis=1)
+    va = np.stack([round_inputs(wl, gen_audio_head(wl, AV_ID, h, M)) for h in heads], axis=1)
+    return qv, ka, va
 
 
 def gen_do_head(wl: Workload, head: int) -> np.ndarray:

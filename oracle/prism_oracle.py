@@ -45,7 +45,11 @@ reading the text supports; each reading is stated where it is used:
      prefix; ties in score go to the smaller block index; no block is forced;
   R8 attention is plain softmax attention of each query token over all tokens of
      its query block's kept blocks, scale 1/sqrt(d), no causal mask; backward
-     treats the kept lists as constants.
+     treats the kept lists as constants;
+  R9 the A2V field is the feature norm of the audio-to-video cross-attention: each
+     video token's query attends (softmax, scale 1/sqrt(d), per head) to every audio
+     token; the field at the token is the L2 norm of its whole output feature, all
+     heads' channels together.
 
 Decisions that floating point makes (which shape, which block) are taken on the
 values in the precision the library stores them in: scores are rounded to fp32
@@ -299,6 +303,25 @@ def bsa_forward(Qb, Kb, Vb, counts, idx, B, heads=None, qblocks=None):
             O[rows, h] = o
             LSE[h, rows] = lse
     return O, LSE
+
+
+def a2v_field(Qv, Ka, Va, rows=None):
+    """The A2V field (R9), from paragraph 1 of the page's block-construction section.
+
+    Qv [N, Hh, d] video queries, Ka / Va [M, Hh, d] audio keys and values.  For every
+    video token n (or only ``rows``): O[n, h] = softmax_m(Qv[n,h] . Ka[m,h] / sqrt(d))
+    weighted sum of Va[m, h]; a2v[n] = sqrt(sum_h |O[n, h]|^2).  Returns (a2v, O) for
+    the rows taken, O as [rows, Hh, d].
+    """
+    N, Hh, d = Qv.shape
+    take = np.arange(N) if rows is None else np.asarray(rows)
+    scale = 1.0 / math.sqrt(d)
+    O = np.zeros((len(take), Hh, d))
+    for h in range(Hh):
+        o, _ = attention_row_block(np.asarray(Qv[take, h], np.float64), np.asarray(Ka[:, h], np.float64),
+                                   np.asarray(Va[:, h], np.float64), scale)
+        O[:, h] = o
+    return np.sqrt((O * O).sum(axis=(1, 2))), O
 
 
 def bsa_backward(Qb, Kb, Vb, O, dO, LSE, counts, idx, B):
