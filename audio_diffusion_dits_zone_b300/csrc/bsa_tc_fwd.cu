@@ -124,28 +124,31 @@ struct FwdSmem {
 constexpr size_t kFwdSmemBytes = sizeof(FwdSmem) + 1024;
 static_assert(kFwdSmemBytes <= 232448, "shared memory budget");
 
-__device__ __forceinline__ int block_of(const int32_t* lst, int it, int nb, bool& ok) {
-  const int j = lst[it];
-  ok = (j >= 0 && j < nb);
+// Key block of step `it`: the kept list's entry, or `it` itself when there is no list
+// (dense: every key block in order).
+__device__ __forceinline__ int block_of(const int32_t* lst, int it, int nbk, bool& ok) {
+  const int j = lst ? lst[it] : it;
+  ok = (j >= 0 && j < nbk);
   return ok ? j : 0;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
-                      float* __restrict__ lse, int64_t ld, int N, const int32_t* __restrict__ counts,
-                      const int32_t* __restrict__ idx, int nb, uint32_t* status) {
+                      float* __restrict__ lse, float* __restrict__ sqn, int64_t ld, int N, int Nk,
+                      const int32_t* __restrict__ counts, const int32_t* __restrict__ idx, int nbq,
+                      int nbk, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x;  // head * nb + query block
-  const int h = item / nb, i = item - h * nb;
-  int cnt = counts[item];
-  if (cnt < 0 || cnt > nb) {
+  const int item = blockIdx.x;  // head * nbq + query block
+  const int h = item / nbq, i = item - h * nbq;
+  int cnt = counts ? counts[item] : nbk;  // no lists: every key block
+  if (cnt < 0 || cnt > nbk) {
     if (threadIdx.x == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
-    cnt = cnt < 0 ? 0 : nb;
+    cnt = cnt < 0 ? 0 : nbk;
   }
-  const int32_t* lst = idx + (size_t)item * nb;
+  const int32_t* lst = counts ? idx + (size_t)item * nbk : nullptr;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.q_full), 1);
@@ -186,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = it % kStages;
         if (it >= kStages && !mbar_wait(smem_u32(&sm.k_empty[st]), ((it / kStages) - 1) & 1, abort, status)) break;
         bool ok;
-        const int j = block_of(lst, it, nb, ok);
+        const int j = block_of(lst, it, nbk, ok);
         const uint32_t bar = smem_u32(&sm.k_full[st]);
         mbar_arrive_expect_tx(bar, kTile);
         tma_load_2d(smem_u32(sm.k[st]), &tmk, h * kD, j * kBN, bar);
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = it % kStages;
         if (it >= kStages && !mbar_wait(smem_u32(&sm.v_empty[st]), ((it / kStages) - 1) & 1, abort, status)) break;
         bool ok;
-        const int j = block_of(lst, it, nb, ok);
+        const int j = block_of(lst, it, nbk, ok);
         const uint32_t bar = smem_u32(&sm.v_full[st]);
         mbar_arrive_expect_tx(bar, kTile);
         tma_load_2d(smem_u32(sm.v[st]), &tmv, h * kD, j * kBN, bar);
@@ -283,17 +286,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    int j_next = cnt > 0 ? lst[0] : 0;  // block indices are read one block ahead
+    int j_next = cnt > 0 ? (lst ? lst[0] : 0) : 0;  // block indices are read one block ahead
     for (int it = 0; it < cnt; ++it) {
       const int b = it % kSBuf;
       const int j_raw = j_next;
-      if (it + 1 < cnt) j_next = lst[it + 1];
+      if (it + 1 < cnt) j_next = lst ? lst[it + 1] : it + 1;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[b]), (it / kSBuf) & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
-      const bool jok = j_raw >= 0 && j_raw < nb;
+      const bool jok = j_raw >= 0 && j_raw < nbk;
       const int j = jok ? j_raw : 0;
-      const int len = jok ? min(kBN, N - j * kBN) : 0;
+      const int len = jok ? min(kBN, Nk - j * kBN) : 0;
       if (!jok && r == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
       // the whole S row: four loads in flight, one wait
       float s[128];
@@ -380,35 +383,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[b]));
     }
     // ---------------------------------------------------------------- epilogue
+    // O (if asked for), lse (if asked for) and |O row|^2 in fp32 before rounding (if asked for)
     const int row = i * kBM + r;
-    __nv_bfloat16* orow = o + (int64_t)row * ld + (int64_t)h * kD;
+    __nv_bfloat16* orow = o ? o + (int64_t)row * ld + (int64_t)h * kD : nullptr;
     if (ok && cnt > 0) {
       // every MMA of the CTA has completed once mma_done flips (it completes once)
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.mma_done), 0, abort, status));
       if (ok) {
         tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
+        float ss = 0.f;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t rr[32];
           tmem_load_row32(lane_base + kOCol + c4 * 32, rr);
           uint32_t pk[16];
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
-            pk[x] = pack_bf16x2(__uint_as_float(rr[2 * x]) * inv, __uint_as_float(rr[2 * x + 1]) * inv);
-          if (row < N) {
+          for (int x = 0; x < 16; ++x) {
+            const float a = __uint_as_float(rr[2 * x]) * inv, b2 = __uint_as_float(rr[2 * x + 1]) * inv;
+            ss = fmaf(a, a, fmaf(b2, b2, ss));
+            pk[x] = pack_bf16x2(a, b2);
+          }
+          if (orow && row < N) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c4 * 32);
 #pragma unroll
             for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
           }
         }
-        if (row < N) lse[(size_t)h * N + row] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+        if (row < N) {
+          if (lse) lse[(size_t)h * N + row] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+          if (sqn) sqn[(size_t)h * N + row] = ss;
+        }
       }
     } else if (cnt == 0 && row < N) {
-      uint4* dst = reinterpret_cast<uint4*>(orow);
+      if (orow) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-      for (int x = 0; x < 16; ++x) dst[x] = make_uint4(0u, 0u, 0u, 0u);
-      lse[(size_t)h * N + row] = -INFINITY;
+        for (int x = 0; x < 16; ++x) dst[x] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (lse) lse[(size_t)h * N + row] = -INFINITY;
+      if (sqn) sqn[(size_t)h * N + row] = 0.f;
     }
   }
   tc_fence_before();
@@ -548,18 +562,25 @@ cudaError_t wait_timeout_selftest_launch(uint64_t limit_ns, int* marker, cudaStr
 cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
                               const int32_t* counts, const int32_t* idx, int nb, void* o, float* lse,
                               cudaStream_t st, uint32_t* status) {
+  return attn_fwd_tc_launch(q, k, v, ld, ld, N, N, Hh, counts, idx, nb, nb, o, lse, nullptr, "bsa_fwd_tc", st,
+                            status);
+}
+
+cudaError_t attn_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int64_t ld_kv, int N,
+                               int Nk, int Hh, const int32_t* counts, const int32_t* idx, int nbq, int nbk, void* o,
+                               float* lse, float* sqn, const char* name, cudaStream_t st, uint32_t* status) {
   CUtensorMap mq, mk, mv;
-  const uint64_t inner = (uint64_t)Hh * kD, row_bytes = (uint64_t)ld * 2;
-  if (!tensor_map_2d_bf16(&mq, q, inner, N, row_bytes, 64, kBM) ||
-      !tensor_map_2d_bf16(&mk, k, inner, N, row_bytes, 64, kBN) ||
-      !tensor_map_2d_bf16(&mv, v, inner, N, row_bytes, 64, kBN))
+  const uint64_t inner = (uint64_t)Hh * kD;
+  if (!tensor_map_2d_bf16(&mq, q, inner, N, (uint64_t)ld * 2, 64, kBM) ||
+      !tensor_map_2d_bf16(&mk, k, inner, Nk, (uint64_t)ld_kv * 2, 64, kBN) ||
+      !tensor_map_2d_bf16(&mv, v, inner, Nk, (uint64_t)ld_kv * 2, 64, kBN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(bsa_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kFwdSmemBytes);
   if (e != cudaSuccess) return e;
-  HookScope hs("bsa_fwd_tc", st);
-  bsa_fwd_tc_kernel<<<(unsigned)Hh * nb, kThreads, kFwdSmemBytes, st>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, ld, N, counts, idx, nb, status);
+  HookScope hs(name, st);
+  bsa_fwd_tc_kernel<<<(unsigned)Hh * nbq, kThreads, kFwdSmemBytes, st>>>(
+      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, sqn, ld, N, Nk, counts, idx, nbq, nbk, status);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,14 @@ cudaError_t row_dot_launch(const void* o, const void* dO, int dtype, int64_t ld,
 cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
                               const int32_t* counts, const int32_t* idx, int nb, void* o, float* lse,
                               cudaStream_t st, uint32_t* status);
+// The same kernel with a key sequence of its own (Nk tokens in nbk blocks, row stride
+// ld_kv) and optional outputs: o, lse and sqn ([Hh][N] fp32, the squared L2 norm of each
+// normalised output row) may each be NULL.  counts == NULL visits every key block.
+cudaError_t attn_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int64_t ld_kv, int N,
+                               int Nk, int Hh, const int32_t* counts, const int32_t* idx, int nbq, int nbk, void* o,
+                               float* lse, float* sqn, const char* name, cudaStream_t st, uint32_t* status);
+// a2v[n] = sqrt(sum_h sqn[h][n]).
+cudaError_t a2v_reduce_launch(const float* sqn, int N, int Hh, float* a2v, cudaStream_t st);
 size_t bwd_tc_rowstats_bytes(int Hh, int nb);
 cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,

@@ -223,6 +223,27 @@ int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32
   return e == cudaSuccess ? (launched(1), ok()) : cuda_fail(e, "prism_bsa_fwd");
 }
 
+int prism_a2v_norm(const void* qv, const void* ka, const void* va, int32_t dtype, int64_t ld_v, int64_t ld_a,
+                   int32_t N, int32_t M, int32_t Hh, int32_t d, void* o, float* a2v, void* ws, size_t* ws_bytes,
+                   void* stream) {
+  if (dtype != PRISM_BF16 || d != 128) return fail(PRISM_EUNSUPPORTED, "prism_a2v_norm is built for bf16, d = 128");
+  if (N < 1 || M < 1 || Hh < 1) return fail(PRISM_EINVAL, "N, M and Hh must be >= 1 (got %d, %d, %d)", N, M, Hh);
+  if (ld_v < (int64_t)Hh * d || ld_a < (int64_t)Hh * d)
+    return fail(PRISM_EINVAL, "row strides %lld, %lld < Hh * d = %d", (long long)ld_v, (long long)ld_a, Hh * d);
+  if (ld_v % 8 != 0 || ld_a % 8 != 0) return fail(PRISM_EINVAL, "row strides must be multiples of 8 elements");
+  int rc;
+  if (ws_query(ws, ws_bytes, ws_round((size_t)Hh * N * sizeof(float)), &rc)) return rc;
+  if (!qv || !ka || !va || !a2v) return fail(PRISM_EINVAL, "NULL pointer");
+  if (!aligned16(qv) || !aligned16(ka) || !aligned16(va) || (o && !aligned16(o)))
+    return fail(PRISM_EINVAL, "qv, ka, va and o must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* sqn = static_cast<float*>(ws);
+  cudaError_t e = prism::attn_fwd_tc_launch(qv, ka, va, ld_v, ld_a, N, M, Hh, nullptr, nullptr, (int)cdiv(N, 128),
+                                            (int)cdiv(M, 128), o, nullptr, sqn, "a2v_attn", st, status_ptr());
+  if (e == cudaSuccess) e = prism::a2v_reduce_launch(sqn, N, Hh, a2v, st);
+  return e == cudaSuccess ? (launched(2), ok()) : cuda_fail(e, "prism_a2v_norm");
+}
+
 int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk, const void* o_blk, const void* do_blk,
                   const float* lse, int32_t dtype, int64_t ld, int32_t N, int32_t Hh, int32_t d, int32_t B,
                   const int32_t* counts, const int32_t* idx, int32_t nb, void* dq, void* dk, void* dv, void* ws,

@@ -31,6 +31,7 @@ _SIGS = {
     "prism_bsa_fwd": [_P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P],
     "prism_bsa_bwd": [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _P, _SZ,
                       _P],
+    "prism_a2v_norm": [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
     "prism_status_check": [_P, ctypes.POINTER(ctypes.c_uint32)],
     "prism_last_error": [],
     "prism_launch_count": [],
@@ -235,6 +236,25 @@ def prism_bsa_fwd(q_blk, k_blk, v_blk, B, counts, idx, o_blk, lse, ws=None, stre
                                    _ptr(counts), _ptr(idx), nb, _ptr(o_blk), _ptr(lse), wsp, nbytes, st)
 
     ws, nbytes = _ws(call, ws, q_blk.device)
+    _check(call(_ptr(ws), ctypes.byref(nbytes)))
+    return ws
+
+
+# --------------------------------------------------------------- A2V field
+def prism_a2v_norm(qv, ka, va, a2v, o=None, ws=None, stream=None):
+    """Audio-to-video cross-attention and its per-token feature norm (a2v [N] fp32).
+    qv [N, Hh, d], ka / va [M, Hh, d] bf16; o ([N, Hh, d] or None) receives the
+    attention output.  Returns the workspace tensor it used."""
+    N, Hh, d = qv.shape
+    M = ka.shape[0]
+    assert _ld(ka) == _ld(va), "ka and va share one row stride"
+    st = _stream(stream)
+
+    def call(wsp, nbytes):
+        return lib().prism_a2v_norm(_ptr(qv), _ptr(ka), _ptr(va), _dtype(qv), _ld(qv), _ld(ka), N, M, Hh, d,
+                                    _ptr(o), _ptr(a2v), wsp, nbytes, st)
+
+    ws, nbytes = _ws(call, ws, qv.device)
     _check(call(_ptr(ws), ctypes.byref(nbytes)))
     return ws
 

@@ -180,7 +180,8 @@ def gen_a2v_inputs(wl: Workload, heads, M: int = AUDIO_TOKENS):
     """Video queries [N, Hh, d] and audio keys / values [M, Hh, d] of the cross-attention,
     rounded like every other input of the workload."""
     heads = list(heads)
-    qv = np.stack([round_inputs(wl, gen_head(wl, AQ_ID, h)) for h in heads], axis=1)
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        qv = np.stack(list(ex.map(lambda h: round_inputs(wl, gen_head(wl, AQ_ID, h)), heads)), axis=1)
     ka = np.stack([round_inputs(wl, gen_audio_head(wl, AK_ID, h, M)) for h in heads], axis=1)
     va = np.stack([round_inputs(wl, gen_audio_head(wl, AV_ID, h, M)) for h in heads], axis=1)
     return qv, ka, va

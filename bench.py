@@ -15,6 +15,11 @@ whole step (forward 4*|b_i|*|b_j|*d + backward 10*|b_i|*|b_j|*d per kept block
 pair, divided by the step time); for N GPUs (torchrun) every rank runs its own
 replica of the workload and value = total work / max-over-ranks time.
 --impl reference times the CPU oracle on the host cores on a bounded sample.
+
+--workload a2v720p times the step upstream of the path instead: the audio-to-video
+cross-attention of the 720p grid's 75,600 video tokens over 157 audio tokens (40
+heads, d = 128, bf16) and its per-token feature norm, the A2V field the zone step
+reads; value = its TFLOP/s (4 * N * M * d * heads per call).
 """
 from __future__ import annotations
 
@@ -338,6 +343,145 @@ def run_e2e(layer, args, world):
             "overlap": "two device layers alternate; H2D, compute and D2H on three streams"}
 
 
+# ------------------------------------------------------------ A2V field
+A2V_METRIC = "A2V cross-attention + feature norm ms/call & TFLOPS (% bf16 peak), 720p"
+
+
+def a2v_config(wl, M):
+    return {"workload": f"a2v720p: audio-to-video cross-attention + per-token feature norm, video grid "
+                        f"T={wl.grid[0]},H={wl.grid[1]},W={wl.grid[2]} ({wl.N} tokens), {M} audio tokens, "
+                        f"{wl.heads} heads, d={wl.d}, bf16",
+            "global_batch": 1, "seq_len": wl.N, "audio_tokens": M, "heads": wl.heads, "head_dim": wl.d,
+            "parallelism": "replicas (one layer per GPU)",
+            "l2": "video queries larger than L2 (774 MB); no flush"}
+
+
+def run_a2v(args, rank, world, local_rank):
+    import torch
+
+    from audio_diffusion_dits_zone_b300 import prism as P
+    from audio_diffusion_dits_zone_b300 import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl, M = synth.WORKLOADS["720p"], synth.AUDIO_TOKENS
+    qv_h, ka_h, va_h = synth.gen_a2v_inputs(wl, range(wl.heads), M)
+    qv, ka, va = (torch.from_numpy(x).to(dev).to(torch.bfloat16) for x in (qv_h, ka_h, va_h))
+    a2v = torch.empty(wl.N, device=dev)
+    ws = P.prism_a2v_norm(qv, ka, va, a2v)
+    for _ in range(args.warmup):
+        P.prism_a2v_norm(qv, ka, va, a2v, ws=ws)
+    if P.status_check() != 0:
+        raise RuntimeError("device status word set in the warm-up")
+    steps = max(args.steps, 20)  # ~0.3 ms per call: enough calls for a stable mean
+    launches0 = P.launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk, P.KernelTimer() as kt:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            P.prism_a2v_norm(qv, ka, va, a2v, ws=ws)
+        t1.record()
+        torch.cuda.synchronize()
+    launches = P.launch_count() - launches0
+    ms = t0.elapsed_time(t1) / steps
+    if world > 1:
+        ms = max_over_ranks(ms, dev)
+    if P.status_check() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    flops = 4.0 * wl.N * M * wl.d * wl.heads              # algorithmic: the audio tokens that exist
+    executed = 4.0 * wl.N * (-(-M // 128) * 128) * wl.d * wl.heads  # the key blocks the tensor cores run
+    pk = peaks()
+    kd = kt.durations()
+    per_kernel = {n: {"ms_per_step": round(sum(v) / steps, 4), "launches_per_step": len(v) // steps,
+                      "ms_per_launch": round(statistics.mean(v), 4)} for n, v in kd.items()}
+    t_attn = per_kernel["a2v_attn"]["ms_per_launch"] * 1e-3
+    achieved = flops / t_attn / 1e12
+    per_kernel["a2v_attn"]["TFLOP/s"] = round(achieved, 2)
+    per_kernel["a2v_attn"]["TFLOP/s_executed_blocks"] = round(executed / t_attn / 1e12, 2)
+    bytes_attn = wl.N * wl.heads * wl.d * 2 + 2 * M * wl.heads * wl.d * 2 + wl.heads * wl.N * 4
+    per_kernel["a2v_attn"]["GB/s"] = round(bytes_attn / t_attn / 1e9, 1)
+    t_red = per_kernel["a2v_reduce"]["ms_per_launch"] * 1e-3
+    per_kernel["a2v_reduce"]["GB/s"] = round((wl.heads * wl.N * 4 + wl.N * 4) / t_red / 1e9, 1)
+    roofline = {"bound": "tensor", "kernel": "a2v_attn", "achieved": round(achieved, 2), "peak": pk["bf16"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4), "traffic": dram_traffic("a2v720p", "a2v_attn"),
+                "peak_note": f"bf16 dense, burst ({pk['source']}; a 0.3 ms kernel between idle gaps); "
+                             f"sustained {pk['bf16_sustained']}",
+                "algorithmic_per_launch": f"{flops:.4e} FLOP ({M} audio tokens; the kernel runs "
+                                          f"{-(-M // 128)} key blocks of 128)"}
+    # end to end through the public call: video queries and audio keys / values copied in
+    # from pinned host memory, the field copied back, every call
+    hq, hk, hv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (qv, ka, va))
+    hq.copy_(qv), hk.copy_(ka), hv.copy_(va)
+    ha = torch.empty(wl.N, dtype=torch.float32, pin_memory=True)
+    e_steps = 5
+    torch.cuda.synchronize()
+    tt = time.perf_counter()
+    for _ in range(e_steps):
+        qv.copy_(hq, non_blocking=True)
+        ka.copy_(hk, non_blocking=True)
+        va.copy_(hv, non_blocking=True)
+        P.prism_a2v_norm(qv, ka, va, a2v, ws=ws)
+        ha.copy_(a2v, non_blocking=True)
+    torch.cuda.synchronize()
+    e_dt = (time.perf_counter() - tt) / e_steps
+    if world > 1:
+        e_dt = max_over_ranks(e_dt, dev)
+    line = {"metric": A2V_METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
+            "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded video queries, audio keys and values; no weights)",
+            "config": a2v_config(wl, M), "per_kernel": per_kernel, "roofline": roofline,
+            "e2e": {"value": round(world * flops / e_dt / 1e12, 3), "unit": UNIT, "ms_per_step": round(e_dt * 1e3, 3),
+                    "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (qv, ka, va))),
+                    "d2h_bytes_per_step": int(a2v.numel() * 4), "steps": e_steps},
+            "gpu_launches": launches, "clocks": clk.summary()}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = a2v_cpu_baseline(qv_h, ka_h, va_h, budget_s=min(args.cpu_seconds, 10.0))
+    return line
+
+
+def a2v_cpu_baseline(qv, ka, va, budget_s=10.0):
+    """The oracle's A2V field, timed on the host cores on rows spread over the grid:
+    chunks of 256 evenly spaced rows, each chunk offset by one row from the last."""
+    import numpy as np
+
+    from oracle import prism_oracle as po
+
+    N, Hh, d = qv.shape
+    M = ka.shape[0]
+    chunk, done, t0 = 256, 0, time.perf_counter()
+    base = np.linspace(0, max(0, N - 1 - chunk), chunk).astype(np.int64)  # + offset < chunk stays below N
+    while time.perf_counter() - t0 < budget_s and done < N:
+        po.a2v_field(qv, ka, va, rows=np.minimum(base + (done // chunk) % chunk, N - 1))
+        done += chunk
+    dt = time.perf_counter() - t0
+    return {"value": round(4.0 * done * M * d * Hh / dt / 1e12, 6), "unit": UNIT, "cores": cpu_threads(),
+            "kind": "oracle", "sample": f"{done} video rows (of {N}) spread over the grid, all {Hh} heads, "
+                                        f"{M} audio tokens; {dt:.1f} s of CPU time; fp64 numpy"}
+
+
+def run_a2v_reference(args):
+    """--impl reference for the A2V workload: the oracle on bounded row samples."""
+    from audio_diffusion_dits_zone_b300 import synth
+
+    wl, M = synth.WORKLOADS["720p"], synth.AUDIO_TOKENS
+    qv, ka, va = synth.gen_a2v_inputs(wl, range(wl.heads), M)
+    a2v_cpu_baseline(qv, ka, va, budget_s=0.5 * max(1, args.warmup))
+    per = max(2.0, min(20.0, 60.0 / max(1, args.steps)))
+    res = [a2v_cpu_baseline(qv, ka, va, budget_s=per) for _ in range(args.steps)]
+    v = statistics.mean(r["value"] for r in res)
+    return {"metric": A2V_METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(4.0 * wl.N * M * wl.d * wl.heads / (v * 1e12) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": a2v_config(wl, M), "impl": "reference",
+            "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": res[0]["cores"], "kind": "oracle",
+                             "sample": f"each step: {res[0]['sample']}"},
+            "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 # ------------------------------------------------------------ the oracle
 def oracle_sample_step(wl, sp, ctx, qblocks):
     """One bounded sample of the step on the CPU oracle: block means and scores of one
@@ -447,15 +591,16 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    a2v = args.workload == "a2v720p"
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args)), flush=True)
+            print(json.dumps(run_a2v_reference(args) if a2v else run_reference(args)), flush=True)
         return
     if world > 1:
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    line = run_ours(args, rank, world, local_rank)
+    line = (run_a2v if a2v else run_ours)(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -173,6 +173,30 @@ int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32
                   void* o_blk, float* lse, void* ws, size_t* ws_bytes, void* stream);
 
 /*
+ * prism_a2v_norm -- the A2V field that prism_zone_shapes takes: the audio-to-video
+ * cross-attention and its per-token feature norm ("Prism: dynamic sparse attention
+ * for 2K joint video-audio generation training", section "Region-adapted block
+ * construction", paragraph 1: each macro-zone uses the feature norm of the
+ * audio-to-video cross-attention, a measure of how strongly the audio drives that
+ * region).  Reading of that passage: for every video token n and head h,
+ *   O[n][h] = sum_m softmax_m(Qv[n][h] . Ka[m][h] / sqrt(d)) Va[m][h],
+ *   a2v[n]  = sqrt(sum_h |O[n][h]|^2)   (L2 norm of the Hh * d output feature).
+ *
+ * qv      [N][Hh][d] video queries, row stride ld_v (raster order).
+ * ka, va  [M][Hh][d] audio keys and values, row stride ld_a.
+ *         dtype PRISM_BF16 and d = 128 only (the tensor-core attention kernel);
+ *         row strides multiples of 8 elements; pointers 16-byte aligned.
+ * o       out [N][Hh][d] bf16, row stride ld_v, or NULL (not written).
+ * a2v     out [N] fp32.
+ * ws      workspace (NULL = size query): Hh * N fp32 squared norms.
+ * Errors: PRISM_EUNSUPPORTED for another dtype or d; PRISM_EINVAL for sizes, strides,
+ * alignment or NULL inputs.  Launches two kernels on `stream`.
+ */
+int prism_a2v_norm(const void* qv, const void* ka, const void* va, int32_t dtype,
+                   int64_t ld_v, int64_t ld_a, int32_t N, int32_t M, int32_t Hh, int32_t d,
+                   void* o, float* a2v, void* ws, size_t* ws_bytes, void* stream);
+
+/*
  * prism_bsa_bwd -- step 5: gradients of block-sparse attention for training (the
  * page trains with Prism BSA switched on).  With the same kept lists as the
  * forward, treated as constants (no gradient through selection):
