@@ -77,6 +77,9 @@ cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64
 cudaError_t attn_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int64_t ld_kv, int N,
                                int Nk, int Hh, const int32_t* counts, const int32_t* idx, int nbq, int nbk, void* o,
                                float* lse, float* sqn, const char* name, cudaStream_t st, uint32_t* status);
+// The cross-attention of the A2V field (a2v.cu): sqn[h][n] = |O[n][h]|^2, O optional.
+cudaError_t a2v_attn_launch(const void* qv, const void* ka, const void* va, int64_t ld_v, int64_t ld_a, int N,
+                            int M, int Hh, void* o, float* sqn, cudaStream_t st, uint32_t* status);
 // a2v[n] = sqrt(sum_h sqn[h][n]).
 cudaError_t a2v_reduce_launch(const float* sqn, int N, int Hh, float* a2v, cudaStream_t st);
 size_t bwd_tc_rowstats_bytes(int Hh, int nb);

@@ -238,8 +238,7 @@ int prism_a2v_norm(const void* qv, const void* ka, const void* va, int32_t dtype
     return fail(PRISM_EINVAL, "qv, ka, va and o must be 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* sqn = static_cast<float*>(ws);
-  cudaError_t e = prism::attn_fwd_tc_launch(qv, ka, va, ld_v, ld_a, N, M, Hh, nullptr, nullptr, (int)cdiv(N, 128),
-                                            (int)cdiv(M, 128), o, nullptr, sqn, "a2v_attn", st, status_ptr());
+  cudaError_t e = prism::a2v_attn_launch(qv, ka, va, ld_v, ld_a, N, M, Hh, o, sqn, st, status_ptr());
   if (e == cudaSuccess) e = prism::a2v_reduce_launch(sqn, N, Hh, a2v, st);
   return e == cudaSuccess ? (launched(2), ok()) : cuda_fail(e, "prism_a2v_norm");
 }

@@ -34,7 +34,10 @@ def check_field(got, ref, what):
 @pytest.mark.parametrize("grid,heads,M", [((5, 8, 16), 2, 157),   # 640 video tokens, audio 128 + 29
                                           ((3, 9, 17), 3, 128),   # 459 video tokens (ragged), one audio block
                                           ((2, 5, 13), 1, 1),     # one audio token: O = Va[0] everywhere
-                                          ((4, 8, 16), 2, 300)])  # three audio blocks, the last one short
+                                          ((3, 8, 16), 2, 40),    # two 32-key chunks, the second short
+                                          ((3, 8, 16), 2, 70),    # three chunks
+                                          ((5, 16, 32), 16, 157),  # 320 tiles: CTAs walk several, across heads
+                                          ((4, 8, 16), 2, 300)])  # three audio blocks (the general kernel)
 def test_a2v_matches_oracle(grid, heads, M):
     wl = workload(grid, heads, 60 + M % 7)
     qv, ka, va = synth.gen_a2v_inputs(wl, range(heads), M)
