@@ -454,7 +454,7 @@ def a2v_cpu_baseline(qv, ka, va, budget_s=10.0):
     M = ka.shape[0]
     chunk, done, t0 = 256, 0, time.perf_counter()
     base = np.linspace(0, max(0, N - 1 - chunk), chunk).astype(np.int64)  # + offset < chunk stays below N
-    while time.perf_counter() - t0 < budget_s and done < N:
+    while time.perf_counter() - t0 < budget_s and done + chunk <= N:
         po.a2v_field(qv, ka, va, rows=np.minimum(base + (done // chunk) % chunk, N - 1))
         done += chunk
     dt = time.perf_counter() - t0
