@@ -15,7 +15,9 @@
 // video tokens), so each head's audio keys and values fit in shared memory next to
 // the video query tiles.  a2v_attn_kernel is persistent: one CTA per SM walks a
 // contiguous range of (head, 128-row query tile) items, loading a head's K and V once
-// and streaming the query tiles through a two-stage ring.  Per tile:
+// (a full 128-row tile for tokens 0-127, a 32-row tile for tokens 128-159) and
+// streaming the query tiles through a four-stage ring, deep enough to keep the DRAM
+// stream of queries busy.  Per tile:
 //   S_x = Q K_x^T for each audio block x (tcgen05, A and B from shared memory; the
 //         last block only as wide as its keys, rounded up to 32);
 //   softmax over all audio tokens at once: the whole S row (up to 160 tokens) in
@@ -43,16 +45,19 @@ constexpr int kHd = 128;                   // head dim
 constexpr uint32_t kBox = 16384;           // 128 rows x 64 bf16, 128-byte swizzled
 constexpr uint32_t kTileB = 2 * kBox;      // 128 x 128 bf16
 constexpr int kMaxChunks = 5;              // audio tokens <= 160: a whole S row in registers
-constexpr int kMaxAudioBlocks = 2;
+constexpr int kQStages = 4;                // video query tiles in flight per CTA
+constexpr int kTailRows = 32;              // the second audio block holds <= 32 tokens
+constexpr uint32_t kTailBox = kTailRows * 128;  // 32 rows x 64 bf16
+constexpr uint32_t kTailB = 2 * kTailBox;
 constexpr uint32_t kOCol = 256, kPCol = 384;
 constexpr float kSl2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
 
 struct A2vSmem {
-  uint8_t k[kMaxAudioBlocks][kTileB];
-  uint8_t v[kMaxAudioBlocks][kTileB];
-  uint8_t q[2][kTileB];
+  uint8_t k0[kTileB], v0[kTileB];   // audio block 0 (up to 128 tokens)
+  uint8_t k1[kTailB], v1[kTailB];   // audio block 1 (tokens 128 .. 159)
+  uint8_t q[kQStages][kTileB];
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t s_full, s_free, p_full, o_full, o_free, fin_s, fin_pv;
   uint32_t tmem_base;
   int abort;
@@ -64,7 +69,8 @@ static_assert(kA2vSmemBytes <= 232448, "shared memory budget");
 template <int NCH>
 __global__ void __launch_bounds__(kA2vThreads, 1)
     a2v_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o, int64_t ld,
+                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmk1,
+                    const __grid_constant__ CUtensorMap tmv1, __nv_bfloat16* __restrict__ o, int64_t ld,
                     float* __restrict__ sqn, int N, int M, int nbq, int nbk, int items, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   A2vSmem& sm = *reinterpret_cast<A2vSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -75,7 +81,7 @@ __global__ void __launch_bounds__(kA2vThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.kv_full), 1);
     mbar_init(smem_u32(&sm.kv_empty), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kQStages; ++s) {
       mbar_init(smem_u32(&sm.q_full[s]), 1);
       mbar_init(smem_u32(&sm.q_empty[s]), 1);
     }
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(kA2vThreads, 1)
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
-      int cur = -1, epoch = -1, armed[2] = {0, 0};
+      int cur = -1, epoch = -1, armed[kQStages] = {};
       for (int t = 0; t < cnt; ++t) {
         const int item = first + t, h = item / nbq, i = item - h * nbq;
         if (h != cur) {  // a new head: its audio K and V, once the last head's products are done
@@ -113,16 +119,20 @@ __global__ void __launch_bounds__(kA2vThreads, 1)
           ++epoch;
           cur = h;
           const uint32_t kvb = smem_u32(&sm.kv_full);
-          mbar_arrive_expect_tx(kvb, 2u * (uint32_t)nbk * kTileB);
-          for (int x = 0; x < nbk; ++x) {
-            tma_load_2d(smem_u32(sm.k[x]), &tmk, h * kHd, x * kRows, kvb);
-            tma_load_2d(smem_u32(sm.k[x]) + kBox, &tmk, h * kHd + 64, x * kRows, kvb);
-            tma_load_2d(smem_u32(sm.v[x]), &tmv, h * kHd, x * kRows, kvb);
-            tma_load_2d(smem_u32(sm.v[x]) + kBox, &tmv, h * kHd + 64, x * kRows, kvb);
+          mbar_arrive_expect_tx(kvb, 2u * kTileB + (nbk > 1 ? 2u * kTailB : 0u));
+          tma_load_2d(smem_u32(sm.k0), &tmk, h * kHd, 0, kvb);
+          tma_load_2d(smem_u32(sm.k0) + kBox, &tmk, h * kHd + 64, 0, kvb);
+          tma_load_2d(smem_u32(sm.v0), &tmv, h * kHd, 0, kvb);
+          tma_load_2d(smem_u32(sm.v0) + kBox, &tmv, h * kHd + 64, 0, kvb);
+          if (nbk > 1) {  // 32-row boxes of the second block
+            tma_load_2d(smem_u32(sm.k1), &tmk1, h * kHd, kRows, kvb);
+            tma_load_2d(smem_u32(sm.k1) + kTailBox, &tmk1, h * kHd + 64, kRows, kvb);
+            tma_load_2d(smem_u32(sm.v1), &tmv1, h * kHd, kRows, kvb);
+            tma_load_2d(smem_u32(sm.v1) + kTailBox, &tmv1, h * kHd + 64, kRows, kvb);
           }
         }
-        const int s = t & 1;
-        if (t >= 2 && !mbar_wait(smem_u32(&sm.q_empty[s]), ((t >> 1) - 1) & 1, abort, status)) break;
+        const int s = t % kQStages;
+        if (t >= kQStages && !mbar_wait(smem_u32(&sm.q_empty[s]), ((t / kQStages) - 1) & 1, abort, status)) break;
         const uint32_t qb = smem_u32(&sm.q_full[s]);
         mbar_arrive_expect_tx(qb, kTileB);
         tma_load_2d(smem_u32(sm.q[s]), &tmq, h * kHd, i * kRows, qb);
@@ -131,7 +141,7 @@ __global__ void __launch_bounds__(kA2vThreads, 1)
       }
       if (*abort) {  // wait (bounded) for the copies still in flight
         if (epoch >= 0) drain_wait(smem_u32(&sm.kv_full), epoch & 1);
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < kQStages; ++s)
           if (armed[s]) drain_wait(smem_u32(&sm.q_full[s]), (armed[s] - 1) & 1);
       }
     }
@@ -143,26 +153,28 @@ __global__ void __launch_bounds__(kA2vThreads, 1)
       const uint32_t id_full = idesc_bf16_f32(kRows, kRows, false, false);
       const uint32_t id_last = idesc_bf16_f32(kRows, n_last, false, false);
       const uint64_t dq0 = smem_desc(smem_u32(sm.q[0]), 16, 1024, kSwizzle128B);
-      const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 16, 1024, kSwizzle128B);
-      auto koff = [](int kk) -> uint32_t { return (kk >> 2) * kBox + (kk & 3) * 32; };
+      const uint64_t dk0 = smem_desc(smem_u32(sm.k0), 16, 1024, kSwizzle128B);
+      const uint64_t dk1 = smem_desc(smem_u32(sm.k1), 16, 1024, kSwizzle128B);
       int cur = -1, epoch = -1;
       bool ok = true;
       for (int t = 0; ok && t < cnt; ++t) {
-        const int item = first + t, h = item / nbq, s = t & 1;
+        const int item = first + t, h = item / nbq, s = t % kQStages;
         if (h != cur) {
           ++epoch;
           cur = h;
           if (!(ok = mbar_wait(smem_u32(&sm.kv_full), epoch & 1, abort, status))) break;
         }
-        if (!(ok = mbar_wait(smem_u32(&sm.q_full[s]), (t >> 1) & 1, abort, status))) break;
+        if (!(ok = mbar_wait(smem_u32(&sm.q_full[s]), (t / kQStages) & 1, abort, status))) break;
         if (t > 0 && !(ok = mbar_wait(smem_u32(&sm.s_free), (t - 1) & 1, abort, status))) break;
         tc_fence_after();
         for (int x = 0; x < nbk; ++x) {
           const uint32_t id = x == nbk - 1 ? id_last : id_full;
+          const uint64_t dkx = x == 0 ? dk0 : dk1;
+          const uint32_t half = x == 0 ? kBox : kTailBox;  // bytes between the two 64-column halves
 #pragma unroll
           for (int kk = 0; kk < kHd / 16; ++kk)
-            mma_ss(tmem + x * kRows, desc_at(dq0, s * kTileB + koff(kk)), desc_at(dk0, x * kTileB + koff(kk)), id,
-                   kk > 0 ? 1u : 0u);
+            mma_ss(tmem + x * kRows, desc_at(dq0, s * kTileB + (kk >> 2) * kBox + (kk & 3) * 32),
+                   desc_at(dkx, (kk >> 2) * half + (kk & 3) * 32), id, kk > 0 ? 1u : 0u);
         }
         tc_commit(smem_u32(&sm.q_empty[s]));
         tc_commit(smem_u32(&sm.s_full));
@@ -176,7 +188,8 @@ __global__ void __launch_bounds__(kA2vThreads, 1)
     if (lane == 0 && cnt > 0) {
       const int k_last = (len_last + 15) >> 4;  // 16-key steps of the last block
       constexpr uint32_t id_pv = idesc_bf16_f32(kRows, kHd, false, true);
-      const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), kBox, 1024, kSwizzle128B);
+      const uint64_t dv0 = smem_desc(smem_u32(sm.v0), kBox, 1024, kSwizzle128B);
+      const uint64_t dv1 = smem_desc(smem_u32(sm.v1), kTailBox, 1024, kSwizzle128B);
       bool ok = true;
       for (int t = 0; ok && t < cnt; ++t) {
         const int item = first + t, h = item / nbq;
@@ -185,8 +198,9 @@ __global__ void __launch_bounds__(kA2vThreads, 1)
         tc_fence_after();
         for (int x = 0; x < nbk; ++x) {
           const int ksteps = x == nbk - 1 ? k_last : kRows / 16;
+          const uint64_t dvx = x == 0 ? dv0 : dv1;
           for (int kk = 0; kk < ksteps; ++kk)
-            mma_ts(tmem + kOCol, tmem + kPCol + x * 64 + kk * 8, desc_at(dv0, x * kTileB + kk * 2048), id_pv,
+            mma_ts(tmem + kOCol, tmem + kPCol + x * 64 + kk * 8, desc_at(dvx, kk * 2048), id_pv,
                    (x > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(&sm.o_full));
@@ -324,14 +338,16 @@ cudaError_t a2v_attn_launch(const void* qv, const void* ka, const void* va, int6
   if (M > 32 * kMaxChunks)  // longer audio: the general kernel, every key block, online softmax
     return attn_fwd_tc_launch(qv, ka, va, ld_v, ld_a, N, M, Hh, nullptr, nullptr, nbq, nbk, o, nullptr, sqn,
                               "a2v_attn", st, status);
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mk1, mv1;
   const uint64_t inner = (uint64_t)Hh * kHd;
   if (!tensor_map_2d_bf16(&mq, qv, inner, N, (uint64_t)ld_v * 2, 64, kRows) ||
       !tensor_map_2d_bf16(&mk, ka, inner, M, (uint64_t)ld_a * 2, 64, kRows) ||
-      !tensor_map_2d_bf16(&mv, va, inner, M, (uint64_t)ld_a * 2, 64, kRows))
+      !tensor_map_2d_bf16(&mv, va, inner, M, (uint64_t)ld_a * 2, 64, kRows) ||
+      !tensor_map_2d_bf16(&mk1, ka, inner, M, (uint64_t)ld_a * 2, 64, kTailRows) ||
+      !tensor_map_2d_bf16(&mv1, va, inner, M, (uint64_t)ld_a * 2, 64, kTailRows))
     return cudaErrorInvalidValue;
-  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, __nv_bfloat16*, int64_t, float*, int, int, int, int, int,
-               uint32_t*) = nullptr;
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, __nv_bfloat16*, int64_t, float*,
+               int, int, int, int, int, uint32_t*) = nullptr;
   switch ((M + 31) >> 5) {
     case 1: kern = a2v_attn_kernel<1>; break;
     case 2: kern = a2v_attn_kernel<2>; break;
@@ -349,7 +365,7 @@ cudaError_t a2v_attn_launch(const void* qv, const void* ka, const void* va, int6
   }
   const int grid = items < sms ? items : sms;
   HookScope hs("a2v_attn", st);
-  kern<<<grid, kA2vThreads, kA2vSmemBytes, st>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(o), ld_v, sqn,
+  kern<<<grid, kA2vThreads, kA2vSmemBytes, st>>>(mq, mk, mv, mk1, mv1, static_cast<__nv_bfloat16*>(o), ld_v, sqn,
                                                           N, M, nbq, nbk, items, status);
   return cudaGetLastError();
 }
