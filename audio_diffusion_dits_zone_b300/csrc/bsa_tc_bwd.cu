@@ -17,10 +17,12 @@
 //   dkdv      one CTA per (head, key block) walking the query blocks that kept it:
 //               S^T = K_j Q_i^T, dP^T = V_j dO_i^T (TMEM),
 //               P^T, dS^T in bf16 into those buffers, dV += P^T dO_i, dK += dS^T Q_i.
-// The softmax-gradient warps work in two halves of 64 columns and release each half
-// as soon as it is written, so the MMAs of the first half overlap the arithmetic of
-// the second.  Warp roles as in the forward kernel: one TMA producer warp, one MMA
-// warp (TMEM owner), four warps that own one TMEM lane (row) each.
+// Both attention kernels have one TMA producer warp, two MMA-issuing threads (one for
+// the products that feed the softmax gradient, one for the accumulating products, so
+// neither stream waits behind the other) and two warpgroups of softmax-gradient warps,
+// each thread owning one TMEM lane (row) and half of the block's columns; each half is
+// released as soon as it is written, so the products of one half overlap the
+// arithmetic of the other.
 #include <cuda.h>
 #include <cuda_bf16.h>
 

@@ -23,6 +23,9 @@
 //               rescaled only when the running row max grows by more than 2^8
 //               (otherwise P is taken against the stale max, which bounds P by 256).
 // TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384,512).
+// The same kernel serves a key sequence of another length (the audio keys of the A2V
+// cross-attention): no lists means every key block in order, and the outputs O and lse
+// are optional while |O row|^2 (fp32, before rounding) can be written instead.
 // The kept lists give block coordinates directly (tokens are already in block
 // order), so gathering a key block is one TMA box coordinate.  Every wait is
 // bounded; on a timeout the CTA drains its copies and MMAs, frees TMEM and exits

@@ -11,7 +11,8 @@
 //               contiguous bytes per row (coalesced); it writes the block-order
 //               copies and the fp32 column sums.  HBM-bound: reads Q, K (, V) once.
 // scores        per head an [nb x d] x [d x nb] fp32 product on CUDA cores
-//               (64 x 64 output tile per CTA, 4 x 4 per thread).  fp32 keeps the
+//               (128 x 128 output tile per CTA, 8 x 8 per thread, the d axis staged
+//               through shared memory 16 at a time, double-buffered).  fp32 keeps the
 //               block order the selection depends on close to the exact one.
 #include <cuda_bf16.h>
 
