@@ -50,7 +50,9 @@ def peaks():
 
 
 def workload_config(wl, sparsity):
-    return {"workload": f"{wl.name}: Prism layer fwd+bwd, T={wl.grid[0]},H={wl.grid[1]},W={wl.grid[2]} "
+    what = "fwd+bwd" if wl.mode == "fwd+bwd" else "forward only (as the config specifies)"
+    groups = f", attention in head groups of {wl.head_group}" if wl.head_group else ""
+    return {"workload": f"{wl.name}: Prism layer {what}{groups}, T={wl.grid[0]},H={wl.grid[1]},W={wl.grid[2]} "
                         f"({wl.N} tokens), {wl.heads} heads, d={wl.d}, {wl.dtype}, B={wl.block}, "
                         f"zones {wl.zone[0]}x{wl.zone[1]}x{wl.zone[2]}, sparsity {sparsity}, CDF {wl.cdf_tau}",
             "global_batch": 1, "seq_len": wl.N, "heads": wl.heads, "head_dim": wl.d, "sparsity": sparsity,
@@ -162,15 +164,19 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     wl = synth.WORKLOADS[args.workload]
     sp = wl.sparsity if args.sparsity is None else args.sparsity
-    layer = PrismLayer(wl, dev, sparsity=sp, train=True)
+    train = wl.mode == "fwd+bwd"
+    layer = PrismLayer(wl, dev, sparsity=sp, train=train)
     layer.load_inputs()
     layer.step()
     if P.status_check() != 0:
         raise RuntimeError("device status word set after the first step")
     fwd_fl, bwd_fl, dense_f, dense_b = layer.flops()
+    if not train:  # forward-only configurations: the step ends with the forward
+        bwd_fl = dense_b = 0.0
     work = fwd_fl + bwd_fl
-    names = ["zone_shapes", "pool_score", "select", "bsa_fwd", "bsa_bwd"]
-    calls = [layer.zone_shapes, layer.pool_score, layer.select, layer.attention_fwd, layer.attention_bwd]
+    names = ["zone_shapes", "pool_score", "select", "bsa_fwd"] + (["bsa_bwd"] if train else [])
+    calls = [layer.zone_shapes, layer.pool_score, layer.select, layer.attention_fwd] + \
+        ([layer.attention_bwd] if train else [])
     for _ in range(args.warmup):
         layer.step()
     torch.cuda.synchronize()
@@ -249,7 +255,7 @@ def run_ours(args, rank, world, local_rank):
                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic}
 
     # ---------------- end to end through the public API, host buffers
-    e2e = run_e2e(layer, args, world)
+    e2e = None if args.no_e2e else run_e2e(layer, args, world)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
@@ -262,7 +268,7 @@ def run_ours(args, rank, world, local_rank):
         "per_call_ms": {n: round(v, 4) for n, v in per_call.items()},
         "per_kernel": per_kernel,
         "attention_tflops": {"bsa_fwd": round(fwd_fl / (per_call["bsa_fwd"] * 1e-3) / 1e12, 2),
-                             "bsa_bwd": round(bwd_fl / (per_call["bsa_bwd"] * 1e-3) / 1e12, 2)},
+                             **({"bsa_bwd": round(bwd_fl / (per_call["bsa_bwd"] * 1e-3) / 1e12, 2)} if train else {})},
         "kept_fraction": round(float(layer.counts.double().mean().item()) / wl.nb, 4),
         "roofline": roofline,
         "e2e": e2e,
@@ -276,8 +282,8 @@ def run_ours(args, rank, world, local_rank):
 
 def run_e2e(layer, args, world):
     """Same step through the public API with host buffers.  Every step copies its
-    inputs (Q, K, V, A2V field, dO) from pinned host memory to the device and its
-    results (O, dQ, dK, dV) back to pinned host memory.  Two device layers take the
+    inputs (Q, K, V, A2V field, and dO when training) from pinned host memory to the
+    device and its results (O, and dQ, dK, dV when training) back to pinned host memory.  Two device layers take the
     steps in turn so that the copies of one step overlap the compute of the other:
     host-to-device copies on one stream, the library calls on a second, device-to-host
     copies on a third, ordered by events (a layer's inputs are refilled only after
@@ -286,13 +292,13 @@ def run_e2e(layer, args, world):
 
     from audio_diffusion_dits_zone_b300.pipeline import PrismLayer
 
-    layers = [layer, PrismLayer(layer.wl, layer.device, sparsity=layer.sparsity, train=True)]
+    layers = [layer, PrismLayer(layer.wl, layer.device, sparsity=layer.sparsity, train=layer.train)]
 
     def ins(L):
-        return [L.q, L.k, L.v, L.a2v, L.do_blk]
+        return [L.q, L.k, L.v, L.a2v] + ([L.do_blk] if L.train else [])
 
     def outs(L):
-        return [L.o_blk, L.dq, L.dk, L.dv]
+        return [L.o_blk] + ([L.dq, L.dk, L.dv] if L.train else [])
 
     h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins(layer)]
     for h, t in zip(h_in, ins(layer)):
@@ -336,6 +342,8 @@ def run_e2e(layer, args, world):
     if world > 1:
         dt = max_over_ranks(dt, layer.device)
     fwd_fl, bwd_fl, _, _ = layer.flops()
+    if not layer.train:
+        bwd_fl = 0.0
     del layers[1]
     return {"value": round(world * (fwd_fl + bwd_fl) / dt / 1e12, 3), "unit": UNIT, "ms_per_step": round(dt * 1e3, 3),
             "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in ins(layer))),
@@ -587,6 +595,7 @@ def main():
     ap.add_argument("--sparsity", type=float, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (extra workloads)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
