@@ -142,18 +142,23 @@ def test_select_on_generated_scores(nb, rows, sp):
             assert np.all(ix[h, i, c[h, i]:] == -7)
 
 
-def test_select_ties_and_flat_rows():
-    nb = 300
-    S = np.concatenate([synth.gen_scores(nb, 100, seed=9, ties=True), np.zeros((100, nb), np.float32),
-                        np.full((100, nb), 3.5, np.float32)]).reshape(1, 300, nb)
+@pytest.mark.parametrize("nb", [300, 1000])  # one warp per row / one CTA per row
+def test_select_ties_and_flat_rows(nb):
+    # select reads [Hh, nb, nb]: 100 rows with ties, 100 flat rows of 0, 100 of 3.5, then generated rows
+    parts = [synth.gen_scores(nb, 100, seed=9, ties=True), np.zeros((100, nb), np.float32),
+             np.full((100, nb), 3.5, np.float32)]
+    if nb > 300:
+        parts.append(synth.gen_scores(nb, nb - 300, seed=10))
+    S = np.concatenate(parts).reshape(1, nb, nb)
     s = torch.from_numpy(S).to(dev)
     counts = torch.empty(1, nb, dtype=torch.int32, device=dev)
     idx = torch.empty(1, nb, nb, dtype=torch.int32, device=dev)
     P.prism_select(s, 0.93, 0.2, counts, idx)
     check_lists(counts.cpu().numpy(), idx.cpu().numpy(), S, 0.93, 0.2)
-    # flat rows: m = ceil(0.2 * 300) = 60 lowest indices (ties go to the smaller index)
-    assert np.all(counts.cpu().numpy()[0, 100:] == 60)
-    assert np.all(idx.cpu().numpy()[0, 150, :60] == np.arange(60))
+    # flat rows: m = ceil(0.2 * nb) lowest indices (ties go to the smaller index); k = ceil(0.07 nb) < m
+    m = -(-nb // 5)
+    assert np.all(counts.cpu().numpy()[0, 100:300] == m)
+    assert np.all(idx.cpu().numpy()[0, 150, :m] == np.arange(m))
 
 
 # ------------------------------------------------------------------ attention
