@@ -3,7 +3,6 @@ agree on the slowest rank's time and on the whole-job throughput."""
 import os
 import socket
 
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 

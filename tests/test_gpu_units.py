@@ -1,8 +1,6 @@
 """GPU parity of each C-ABI call on its own, against the CPU oracle, on seeded inputs
 small enough for the oracle to finish in seconds while still spanning several
 tiles and a ragged tail."""
-import math
-
 import numpy as np
 import pytest
 import torch
