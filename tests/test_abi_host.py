@@ -105,3 +105,31 @@ def test_pool_score_argument_rules(L):
     # scores without block means
     assert L.prism_pool_score(p, p, p, P.PRISM_BF16, 1024, None, 1000, 8, 128, 128, None, None, None, 0, None, None,
                               p, None) == P.PRISM_EINVAL
+
+
+def test_a2v_norm_argument_rules_and_workspace(L):
+    p = ctypes.c_void_p(256)
+    n = ctypes.c_size_t(0)
+    # workspace: one fp32 squared norm per (head, video token)
+    assert L.prism_a2v_norm(p, p, p, P.PRISM_BF16, 5120, 5120, 75600, 157, 40, 128, None, p, None, ctypes.byref(n),
+                            None) == P.PRISM_OK
+    assert n.value >= 40 * 75600 * 4 and n.value % 256 == 0
+    # only bf16 with d = 128 is built
+    assert L.prism_a2v_norm(p, p, p, P.PRISM_F32, 5120, 5120, 75600, 157, 40, 128, None, p, None, _sz(),
+                            None) == P.PRISM_EUNSUPPORTED
+    assert L.prism_a2v_norm(p, p, p, P.PRISM_BF16, 2560, 2560, 75600, 157, 40, 64, None, p, None, _sz(),
+                            None) == P.PRISM_EUNSUPPORTED
+    # sizes, strides, pointers
+    assert L.prism_a2v_norm(p, p, p, P.PRISM_BF16, 5120, 5120, 75600, 0, 40, 128, None, p, None, _sz(),
+                            None) == P.PRISM_EINVAL
+    assert L.prism_a2v_norm(p, p, p, P.PRISM_BF16, 4096, 5120, 75600, 157, 40, 128, None, p, None, _sz(),
+                            None) == P.PRISM_EINVAL
+    assert L.prism_a2v_norm(p, p, p, P.PRISM_BF16, 5124, 5120, 75600, 157, 40, 128, None, p, None, _sz(),
+                            None) == P.PRISM_EINVAL
+    ws = ctypes.c_void_p(1 << 20)
+    big = ctypes.c_size_t(1 << 30)
+    assert L.prism_a2v_norm(None, p, p, P.PRISM_BF16, 5120, 5120, 75600, 157, 40, 128, None, p, ws,
+                            ctypes.byref(big), None) == P.PRISM_EINVAL
+    assert L.prism_a2v_norm(ctypes.c_void_p(258), p, p, P.PRISM_BF16, 5120, 5120, 75600, 157, 40, 128, None, p, ws,
+                            ctypes.byref(big), None) == P.PRISM_EINVAL
+    assert b"aligned" in L.prism_last_error()
