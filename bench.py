@@ -493,8 +493,8 @@ def run_a2v_reference(args):
 # ------------------------------------------------------------ the oracle
 def oracle_sample_step(wl, sp, ctx, qblocks):
     """One bounded sample of the step on the CPU oracle: block means and scores of one
-    head, selection of the sampled query blocks, and their attention forward and
-    backward (dQ of the sample, dK/dV contributions of the sample)."""
+    head, selection of the sampled query blocks, and their attention forward and, for
+    training workloads, backward (dQ of the sample, dK/dV contributions of the sample)."""
     import numpy as np
 
     from oracle import prism_oracle as po
@@ -513,6 +513,8 @@ def oracle_sample_step(wl, sp, ctx, qblocks):
         lens = np.minimum(wl.block, wl.N - kept * wl.block)
         pairs += int(lens.sum()) * min(wl.block, wl.N - i * wl.block)
     po.bsa_forward(Qb, Kb, Vb, counts, idx, wl.block, qblocks=qblocks)
+    if wl.mode != "fwd+bwd":
+        return 4.0 * pairs * wl.d
     po.bsa_backward_sampled(Qb, Kb, Vb, dOb, counts, idx, wl.block, 0, qblocks, [])
     return 14.0 * pairs * wl.d
 
@@ -553,7 +555,8 @@ def cpu_baseline(wl, sp, budget_s=20.0, head=0):
         done += 2
     dt = time.perf_counter() - t0
     return {"value": round(work / dt / 1e12, 6), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"head {head}: block means/scores, selection and attention fwd+bwd of {done} query blocks "
+            "sample": f"head {head}: block means/scores, selection and attention "
+                      f"{'fwd+bwd' if wl.mode == 'fwd+bwd' else 'forward'} of {done} query blocks "
                       f"(of {wl.nb}) spread over the sequence; {dt:.1f} s of CPU time; zone statistics "
                       f"over this head's channels done once outside the timing"}
 
@@ -574,7 +577,8 @@ def run_reference(args):
         work += oracle_sample_step(wl, sp, ctx, b)
     dt = time.perf_counter() - t0
     v = work / dt / 1e12
-    sample = (f"each step: head 0, block means/scores, selection and attention fwd+bwd of {per} query blocks "
+    sample = (f"each step: head 0, block means/scores, selection and attention "
+              f"{'fwd+bwd' if wl.mode == 'fwd+bwd' else 'forward'} of {per} query blocks "
               f"(of {wl.nb}); fp64 numpy")
     return {"metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
