@@ -75,22 +75,33 @@ def job_throughput(work_per_rank: float, world: int, seconds: float) -> float:
     return world * work_per_rank / seconds / 1e12
 
 
-def dram_traffic(workload, kernel):
-    """DRAM bytes (read + write) per launch of `kernel` on `workload`, from the ncu
-    summary table in profiles/traffic.md (rows "| workload | kernel | bytes | ... |"),
-    or None when no capture of the kernel as it stands is recorded."""
-    path = os.path.join(ROOT, "profiles", "traffic.md")
+def source_sha1(rel):
+    """SHA-1 of a source file of the repository (to tie a capture to the code it measured)."""
+    import hashlib
+
+    path = os.path.join(ROOT, rel)
     if not os.path.exists(path):
         return None
+    with open(path, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+def dram_traffic(workload, kernel):
+    """(bytes, note): DRAM bytes (read + write) per launch of `kernel` on `workload` from
+    the ncu capture recorded in profiles/traffic.json, and where that figure comes from.
+    bytes is None when no capture is recorded, or when the kernel's source file has
+    changed since the capture (its SHA-1 differs from the one recorded with it)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None, "no ncu capture recorded"
     with open(path) as f:
-        for line in f:
-            cells = [c.strip() for c in line.strip().strip("|").split("|")]
-            if len(cells) >= 3 and cells[0] == workload and cells[1] == kernel:
-                try:
-                    return float(cells[2])
-                except ValueError:
-                    return None
-    return None
+        rows = json.load(f)["captures"]
+    for r in rows:
+        if r["workload"] == workload and r["kernel"] == kernel:
+            if source_sha1(r["source"]) != r["source_sha1"]:
+                return None, f"{r['source']} changed since the ncu capture"
+            return float(r["bytes_per_launch"]), f"ncu capture: {r['capture']}"
+    return None, "no ncu capture of this kernel as it stands"
 
 
 # ---------------------------------------------------------------- clocks
@@ -219,9 +230,11 @@ def run_ours(args, rank, world, local_rank):
     pairs = fwd_fl / (4.0 * wl.d)
     C = wl.heads * wl.d
     kept = int(layer.counts.sum().item())
+    npad = wl.nb * wl.block
     algo = {
         "bsa_fwd_tc": ("tensor", 4.0 * pairs * wl.d), "bsa_dq_tc": ("tensor", 6.0 * pairs * wl.d),
-        "bsa_dkdv_tc": ("tensor", 8.0 * pairs * wl.d),
+        "bsa_dkdv_tc": ("tensor", 8.0 * pairs * wl.d), "bsa_bwd_tc": ("tensor", 10.0 * pairs * wl.d),
+        "dq_convert": ("hbm", wl.heads * npad * wl.d * 4.0 + wl.N * C * 2.0),
         "zone_tma": ("hbm", wl.N * C * 2.0), "zone_partial": ("hbm", wl.N * C * 2.0),
         "pool_gather": ("hbm", 6.0 * wl.N * C * 2 + 2.0 * wl.heads * wl.nb * wl.d * 4),
         "scores": ("hbm", wl.heads * wl.nb ** 2 * 4.0 + 2.0 * wl.heads * wl.nb * wl.d * 4),
@@ -233,6 +246,7 @@ def run_ours(args, rank, world, local_rank):
             t = per_kernel[n]["ms_per_step"] * 1e-3
             if bound == "tensor":
                 per_kernel[n]["TFLOP/s"] = round(w / t / 1e12, 2)
+                per_kernel[n]["frac_bf16_burst"] = round(w / t / 1e12 / pk["bf16"], 4)
                 per_kernel[n]["frac_bf16_sustained"] = round(w / t / 1e12 / pk["bf16_sustained"], 4)
             else:
                 per_kernel[n]["GB/s"] = round(w / t / 1e9, 1)
@@ -241,18 +255,21 @@ def run_ours(args, rank, world, local_rank):
     bound, w = algo.get(dom, ("tensor", 0.0))
     t_launch = per_kernel[dom]["ms_per_launch"] * 1e-3
     w_launch = w / max(1, per_kernel[dom]["launches_per_step"])
-    traffic = dram_traffic(wl.name, dom)
+    traffic, traffic_note = dram_traffic(wl.name, dom)
     if bound == "tensor":
+        # the burst peak: kernels of this step run above the seconds-long sustained figure
         achieved = w_launch / t_launch / 1e12
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": pk["bf16_sustained"],
-                    "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sustained"], 4), "traffic": traffic,
-                    "peak_note": f"bf16 dense, sustained ({pk['source']}); burst {pk['bf16']}",
-                    "frac_of_burst": round(achieved / pk["bf16"], 4),
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": pk["bf16"],
+                    "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4), "traffic": traffic,
+                    "traffic_note": traffic_note,
+                    "peak_note": f"bf16 dense, burst ({pk['source']}); sustained {pk['bf16_sustained']}",
+                    "frac_of_sustained": round(achieved / pk["bf16_sustained"], 4),
                     "algorithmic_per_launch": f"{w_launch:.4e} FLOP"}
     else:
         achieved = w_launch / t_launch / 1e9
         roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic}
+                    "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
+                    "traffic_note": traffic_note}
 
     # ---------------- end to end through the public API, host buffers
     e2e = None if args.no_e2e else run_e2e(layer, args, world)
@@ -264,7 +281,8 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_layer": round(ms, 3),
         "tflops_executed": round(work / (ms * 1e-3) / 1e12, 3),
         "tflops_dense_equivalent": round((dense_f + dense_b) / (ms * 1e-3) / 1e12, 3),
-        "pct_bf16_peak_executed": round(100 * work / (ms * 1e-3) / 1e12 / pk["bf16_sustained"], 2),
+        "pct_bf16_peak_executed": round(100 * work / (ms * 1e-3) / 1e12 / pk["bf16"], 2),
+        "pct_bf16_sustained_executed": round(100 * work / (ms * 1e-3) / 1e12 / pk["bf16_sustained"], 2),
         "per_call_ms": {n: round(v, 4) for n, v in per_call.items()},
         "per_kernel": per_kernel,
         "attention_tflops": {"bsa_fwd": round(fwd_fl / (per_call["bsa_fwd"] * 1e-3) / 1e12, 2),
@@ -413,8 +431,10 @@ def run_a2v(args, rank, world, local_rank):
     per_kernel["a2v_attn"]["GB/s"] = round(bytes_attn / t_attn / 1e9, 1)
     t_red = per_kernel["a2v_reduce"]["ms_per_launch"] * 1e-3
     per_kernel["a2v_reduce"]["GB/s"] = round((wl.heads * wl.N * 4 + wl.N * 4) / t_red / 1e9, 1)
+    traffic, traffic_note = dram_traffic("a2v720p", "a2v_attn")
     roofline = {"bound": "tensor", "kernel": "a2v_attn", "achieved": round(achieved, 2), "peak": pk["bf16"],
-                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4), "traffic": dram_traffic("a2v720p", "a2v_attn"),
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4), "traffic": traffic,
+                "traffic_note": traffic_note,
                 "peak_note": f"bf16 dense, burst ({pk['source']}; a 0.3 ms kernel between idle gaps); "
                              f"sustained {pk['bf16_sustained']}",
                 "algorithmic_per_launch": f"{flops:.4e} FLOP ({M} audio tokens; the kernel runs "
@@ -493,8 +513,10 @@ def run_a2v_reference(args):
 # ------------------------------------------------------------ the oracle
 def oracle_sample_step(wl, sp, ctx, qblocks):
     """One bounded sample of the step on the CPU oracle: block means and scores of one
-    head, selection of the sampled query blocks, and their attention forward and, for
-    training workloads, backward (dQ of the sample, dK/dV contributions of the sample)."""
+    head, selection of the sampled query blocks, their attention forward and, for
+    training workloads, the backward contributions of those query blocks (their dQ and
+    their shares of dK and dV for every kept key block).  Returns the algorithmic
+    FLOPs of what it ran: 4 |b_i| |b_j| d per kept pair forward, 10 backward."""
     import numpy as np
 
     from oracle import prism_oracle as po
@@ -512,10 +534,10 @@ def oracle_sample_step(wl, sp, ctx, qblocks):
         idx[0, i, : kept.size] = kept
         lens = np.minimum(wl.block, wl.N - kept * wl.block)
         pairs += int(lens.sum()) * min(wl.block, wl.N - i * wl.block)
-    po.bsa_forward(Qb, Kb, Vb, counts, idx, wl.block, qblocks=qblocks)
+    O, L = po.bsa_forward(Qb, Kb, Vb, counts, idx, wl.block, qblocks=qblocks)
     if wl.mode != "fwd+bwd":
         return 4.0 * pairs * wl.d
-    po.bsa_backward_sampled(Qb, Kb, Vb, dOb, counts, idx, wl.block, 0, qblocks, [])
+    po.bsa_backward(Qb, Kb, Vb, O, dOb, L, counts, idx, wl.block, qblocks=qblocks)
     return 14.0 * pairs * wl.d
 
 
@@ -556,7 +578,7 @@ def cpu_baseline(wl, sp, budget_s=20.0, head=0):
     dt = time.perf_counter() - t0
     return {"value": round(work / dt / 1e12, 6), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
             "sample": f"head {head}: block means/scores, selection and attention "
-                      f"{'fwd+bwd' if wl.mode == 'fwd+bwd' else 'forward'} of {done} query blocks "
+                      f"{'fwd+bwd (dQ and the dK/dV contributions of the sampled query blocks)' if wl.mode == 'fwd+bwd' else 'forward'} of {done} query blocks "
                       f"(of {wl.nb}) spread over the sequence; {dt:.1f} s of CPU time; zone statistics "
                       f"over this head's channels done once outside the timing"}
 

@@ -324,11 +324,13 @@ def a2v_field(Qv, Ka, Va, rows=None):
     return np.sqrt((O * O).sum(axis=(1, 2))), O
 
 
-def bsa_backward(Qb, Kb, Vb, O, dO, LSE, counts, idx, B):
+def bsa_backward(Qb, Kb, Vb, O, dO, LSE, counts, idx, B, heads=None, qblocks=None):
     """Step 5: dQ, dK, dV for the same kept lists (R8).
 
     P = exp(S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
     dS = P * (dP - D), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d).
+    ``heads`` / ``qblocks`` restrict the work to the contributions of a sample of
+    query blocks (dK and dV then hold only those contributions).
     """
     N, Hh, d = Qb.shape
     nb = -(-N // B)
@@ -336,8 +338,8 @@ def bsa_backward(Qb, Kb, Vb, O, dO, LSE, counts, idx, B):
     dQ = np.zeros((N, Hh, d))
     dK = np.zeros((N, Hh, d))
     dV = np.zeros((N, Hh, d))
-    for h in range(Hh):
-        for i in range(nb):
+    for h in (range(Hh) if heads is None else heads):
+        for i in (range(nb) if qblocks is None else qblocks):
             rows = np.arange(i * B, min((i + 1) * B, N))
             cols = kept_tokens(idx[h, i, : counts[h, i]], B, N)
             if cols.size == 0:

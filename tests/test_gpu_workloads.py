@@ -13,7 +13,7 @@ from audio_diffusion_dits_zone_b300 import prism as P
 from audio_diffusion_dits_zone_b300 import synth
 from audio_diffusion_dits_zone_b300.pipeline import PrismLayer
 from oracle import prism_oracle as po
-from parity import attn_close, check_lists, score_error_bound
+from parity import attn_close, check_lists, compare_perm_by_zone, record, score_error_bound, tie_budget
 
 pytestmark = pytest.mark.gpu
 
@@ -57,37 +57,69 @@ def gpu_layer(name, sparsity):
 
 
 def check_zones(layer, name):
+    wl = synth.WORKLOADS[name]
     zs, perm, cost = oracle_zones(name)
     g = layer.zone_shape.cpu().numpy()
     differ = np.nonzero(g != zs)[0]
     for z in differ:   # only near-ties of the fp32 cost may differ
         assert cost[z, g[z]] - cost[z].min() <= 1e-4, (z, g[z], zs[z], cost[z])
-    if differ.size == 0:
-        assert np.array_equal(layer.perm.cpu().numpy(), perm)
+    compared = compare_perm_by_zone(layer.perm.cpu().numpy(), perm, g, zs, wl.grid, wl.zone)
+    assert compared == len(zs) - differ.size
     return zs, perm, differ.size
 
 
-def check_head(layer, wl, h, perm, sp, qblocks, grad_blocks=()):
+def nearest(cands, ok, n_valid, count):
+    """Up to `count` distinct indices: each candidate if ok(i), else the nearest index that is."""
+    out = []
+    for c in cands:
+        for dist in range(n_valid):
+            hit = next((i for i in (c - dist, c + dist) if 0 <= i < n_valid and ok(i) and i not in out), None)
+            if hit is not None:
+                out.append(hit)
+                break
+        if len(out) == count:
+            break
+    return out
+
+
+def check_head(layer, wl, h, perm, sp, qblocks, grad_blocks=None, case=""):
+    """Scores, kept lists, forward (and with grad_blocks, gradients) of head h against the
+    oracle.  Attention is compared on query blocks whose kept list equals the oracle's
+    and, for dK / dV, on key blocks that only such query blocks keep: there both sides
+    run the same mask, so the comparison is element by element and never skipped."""
     Q, K, V = oracle_head(wl, h, perm)
-    qbar, kbar, S = po.block_mean(Q, wl.block), po.block_mean(K, wl.block), None
+    qbar, kbar = po.block_mean(Q, wl.block), po.block_mean(K, wl.block)
     S = po.block_scores(qbar, kbar)
     gS = layer.scores[h].cpu().numpy()[None]
     bound = score_error_bound(qbar, kbar, wl.d)
-    assert np.all(np.abs(gS - S) <= bound[:, :, None] + 1e-7), float(np.abs(gS - S).max())
+    err = np.abs(gS - S)
+    assert np.all(err <= bound[:, :, None] + 1e-7), float(err.max())
     counts = layer.counts[h:h + 1].cpu().numpy()
     idx = layer.idx[h:h + 1].cpu().numpy()
-    n, exact, tie = check_lists(counts, idx, S, sp, wl.cdf_tau, score_tol=bound)
+    stats, same = check_lists(counts, idx, S, sp, wl.cdf_tau, score_err=err.max(-1))
+    assert stats["score"] + stats["mass"] <= tie_budget(stats["rows"]), stats
     ocounts, oidx = po.select(S, sp, wl.cdf_tau)
-    same = [i for i in range(wl.nb) if np.array_equal(idx[0, i, : counts[0, i]], oidx[0, i, : ocounts[0, i]])]
-    rows = [i for i in qblocks if i in same]
+    match = lambda i: (0, i) in same  # noqa: E731
+    rows = nearest(qblocks, match, wl.nb, len(qblocks))
+    assert len(rows) >= 3, rows
     O, L = po.bsa_forward(Q, K, V, ocounts, oidx, wl.block, qblocks=rows)
     for i in rows:
         r = slice(i * wl.block, min((i + 1) * wl.block, wl.N))
         attn_close(layer.o_blk[r, h].float().cpu().numpy(), O[r, 0], what=f"O h={h} i={i}")
         np.testing.assert_allclose(layer.lse[h, r].cpu().numpy(), L[0, r], atol=2e-3)
-    if grad_blocks and len(same) == wl.nb:
+    entry = {"head": h, "sparsity": sp, **stats, "fwd_blocks": rows}
+    if grad_blocks is not None:
+        qc, kc = grad_blocks
+        # key blocks kept by any query block whose list differs (on either side)
+        tainted = set()
+        for i in range(wl.nb):
+            if not match(i):
+                tainted.update(oidx[0, i, : ocounts[0, i]].tolist())
+                tainted.update(idx[0, i, : counts[0, i]].tolist())
+        qb = nearest(qc, match, wl.nb, len(qc))
+        kb = nearest(kc, lambda j: j not in tainted, wl.nb, len(kc))
+        assert len(qb) >= 3 and len(kb) >= 2, (qb, kb)
         dO = synth.gen_heads(wl, synth.DO_ID, [h])[0].astype(np.float64)[:, None, :]
-        qb, kb = grad_blocks
         dq, dk, dv = po.bsa_backward_sampled(Q, K, V, dO, ocounts, oidx, wl.block, 0, qb, kb)
         for i in qb:
             r = slice(i * wl.block, min((i + 1) * wl.block, wl.N))
@@ -96,7 +128,9 @@ def check_head(layer, wl, h, perm, sp, qblocks, grad_blocks=()):
             r = slice(j * wl.block, min((j + 1) * wl.block, wl.N))
             attn_close(layer.dk[r, h].float().cpu().numpy(), dk[j], what=f"dK h={h} j={j}")
             attn_close(layer.dv[r, h].float().cpu().numpy(), dv[j], what=f"dV h={h} j={j}")
-    return n, exact, tie, len(rows)
+        entry.update({"dq_blocks": qb, "dkdv_blocks": kb, "tainted_key_blocks": len(tainted)})
+    record(case, entry)
+    return stats, rows
 
 
 @pytest.mark.parametrize("name", ["720p", "1080p", "2k"])
@@ -104,13 +138,12 @@ def test_forward_workload(name):
     wl = synth.WORKLOADS[name]
     layer = gpu_layer(name, wl.sparsity)
     zs, perm, nd = check_zones(layer, name)
-    print(f"{name}: {nd} zone shapes differ within the tie tolerance")
+    record(f"{name} zones", {"zones": len(zs), "shape_near_ties": int(nd)})
     rng = np.random.default_rng(wl.cid)
     for h in (0, wl.heads - 1):
         qblocks = sorted(set(rng.choice(wl.nb - 1, 3, replace=False).tolist()) | {0, wl.nb - 1})
-        n, exact, tie, checked = check_head(layer, wl, h, perm, wl.sparsity, qblocks)
-        print(f"{name} head {h}: lists {exact}/{n} exact, {tie} near-ties accepted; {checked} blocks compared")
-        assert checked >= 3
+        stats, rows = check_head(layer, wl, h, perm, wl.sparsity, qblocks, case=name)
+        print(f"{name} head {h}: {stats}; forward compared on blocks {rows}")
     # property at any size: every kept list holds at least k blocks and at most nb, ascending
     c = layer.counts.cpu().numpy()
     assert c.min() >= po.keep_count_topk(wl.nb, wl.sparsity) and c.max() <= wl.nb
@@ -127,8 +160,8 @@ def test_training_workload(sp):
     h = 3
     qb = [0, wl.nb // 2, wl.nb - 1]
     kb = [wl.nb // 3, wl.nb - 1]
-    n, exact, tie, checked = check_head(layer, wl, h, perm, sp, qb, grad_blocks=(qb, kb))
-    print(f"train720p s={sp}: lists {exact}/{n} exact, {tie} near-ties; fwd blocks {checked}")
+    stats, rows = check_head(layer, wl, h, perm, sp, qb, grad_blocks=(qb, kb), case=f"{name} s={sp}")
+    print(f"train720p s={sp}: {stats}; forward compared on blocks {rows}")
     # dV summed over all key tokens equals dO summed over all query tokens (rows of P sum to 1)
     dv_sum = layer.dv[:, h].double().sum(0).cpu().numpy()
     do_sum = layer.do_blk[:, h].double().sum(0).cpu().numpy()

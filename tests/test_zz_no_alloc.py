@@ -48,10 +48,11 @@ def test_noalloc_zone_shapes_match_workspace_version_twice():
 
 
 def test_noalloc_rejects_grids_beyond_its_scratch():
-    # 700 zones x 40,000 channels would need about 5 MB of scratch: refused before any device work
-    p = ctypes.c_void_p(256)
+    # 700 zones x 40,000 channels would need about 5 MB of scratch: refused before any
+    # device work.  The device pointers are NULL, so a regression of the size check
+    # ends in the NULL-pointer refusal (PRISM_EINVAL), never in a launch.
     shapes = (ctypes.c_int32 * 12)(1, 8, 16, 2, 8, 8, 4, 4, 8, 8, 4, 4)
-    rc = P.lib().prism_zone_shapes_noalloc(p, P.PRISM_BF16, 40000, 40000, p, 21, 90, 160, 3, 9, 16, shapes, 4,
-                                           p, p, None)
+    rc = P.lib().prism_zone_shapes_noalloc(None, P.PRISM_BF16, 40000, 40000, None, 21, 90, 160, 3, 9, 16, shapes,
+                                           4, None, None, None)
     assert rc == P.PRISM_EUNSUPPORTED
     assert b"scratch" in P.lib().prism_last_error()
