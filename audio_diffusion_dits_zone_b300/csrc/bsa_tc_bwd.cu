@@ -26,6 +26,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstddef>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -42,15 +44,22 @@ constexpr float kScale = 0.08838834764831845f;                      // 1 / sqrt(
 
 // ------------------------------------------------------------------- prep
 // 16 threads per (head, padded row), 8 channels (one 16-byte load of O and of dO) each.
+// With dqacc != NULL it also clears the fused kernel's fp32 dQ accumulator
+// ([npad][Hh * d]): each thread zeroes the 8 accumulator channels it owns.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dO,
                                                        const float* __restrict__ lse, int64_t ld, int N, int Hh,
-                                                       int npad, float* __restrict__ L2, float* __restrict__ Dp) {
+                                                       int npad, float* __restrict__ L2, float* __restrict__ Dp,
+                                                       float* __restrict__ dqacc) {
   const int64_t gid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
   const int sub = threadIdx.x & 15;
   if (gid >= (int64_t)Hh * npad) return;  // 16-lane groups are whole: the group exits together
   // rows fastest within a head, so consecutive groups read consecutive token rows
   const int h = (int)(gid / npad), r = (int)(gid - (int64_t)h * npad);
+  if (dqacc) {
+    float4* z = reinterpret_cast<float4*>(dqacc + (int64_t)r * Hh * kD + (int64_t)h * kD + sub * 8);
+    z[0] = z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float s = 0.f;
   if (r < N) {
     const int64_t off = (int64_t)r * ld + (int64_t)h * kD + sub * 8;
@@ -662,14 +671,433 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   }
 }
 
+// ------------------------------------------------------- fused dK, dV, dQ
+// One CTA per (head, key block j) walking the query blocks that kept j, like dkdv,
+// that also forms dQ: per query half x of query block i,
+//   S^T_x = K_j Q_x^T, dP^T_x = V_j dO_x^T (TMEM, N = 64), P^T_x and dS^T_x (bf16),
+//   dV += P^T_x dO_x, dK += dS^T_x Q_x (A from TMEM), and
+//   dQ_x^T = K_j^T dS_x^T (M = 128 channels, N = 64 queries, K = 128 keys; both
+//   operands MN-major in shared memory: K_j's tile as it was loaded, dS^T_x written
+//   by the softmax warps in the same 128-byte-swizzled layout),
+// and adds dQ_x into an fp32 accumulator in global memory ([npad][Hh * d]) with
+// 16-byte reductions issued straight from registers.  Five tile products per kept pair instead of the seven of the split
+// kernels (whose dq kernel recomputes S and dP).  The reduce-adds make dQ's summation
+// order, and so its last bits, depend on scheduling.
+//
+// Warps: 0 TMA producer, 1 issuer of S^T and dP^T (TMEM owner), 2 issuer of dV, dK
+// and dQ^T, 3 idle; 4-7 softmax gradient of query rows 0-63 (half a) of every query
+// block, 8-11 of rows 64-127 (half b), a thread per key row (its TMEM lane); 12-15
+// the dQ drain, a thread per channel (TMEM lane of dQ^T).
+constexpr int kFusedThreads = 512;
+
+struct FusedSmem {
+  uint8_t k[kTile];
+  uint8_t v[kTile];
+  QdoStage st[2];
+  // [query half]: dS^T_x (128 key rows x 64 queries bf16, 128-byte swizzle), the B
+  // operand of dQ_x^T
+  uint8_t ds[2][kHalf];
+  float l2[2][kB];  // lse * log2(e) of the stage's query rows
+  float dr[2][kB];  // D of the stage's query rows
+  uint64_t kv_full;
+  uint64_t qdo_full[2], qdo_empty[2];
+  uint64_t s_full[2], dp_full[2];  // [query half]: S^T, dP^T computed
+  uint64_t p_full[2], ds_full[2];  // [query half]: P^T, dS^T written
+  uint64_t v_done[2], k_done[2];   // [query half]: dV has read P^T / dK has read dS^T
+  uint64_t dq_full[2];             // [query half]: dQ^T computed (dS^T tile read)
+  uint64_t dq_free[2];             // [query half]: dQ^T loaded by the drain (TMEM free)
+  uint64_t acc_done, in_done;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kFusedSmemBytes = sizeof(FusedSmem);
+static_assert(kFusedSmemBytes <= 232448, "shared memory budget");
+static_assert(offsetof(FusedSmem, ds) % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+// TMEM: S^T_a [0,64) S^T_b [64,128) dP^T_a [128,192) dP^T_b [192,256) dV [256,384)
+// dK [384,512).  In the S^T_x columns the softmax writes P^T_x (bf16) over the first
+// 32 and dS^T_x over the last 32; dQ_x^T is computed into the dP^T_x columns once the
+// softmax has loaded them.  Issuer 1: S^T_a, S^T_b (each once dV and dK of the previous
+// pair have read that half's P^T, dS^T), then dP^T_a, dP^T_b (each once the drain has
+// loaded the previous dQ^T of that half).  Issuer 2 per half: dV once P^T is written;
+// dK and dQ^T once dS^T is written.
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    bsa_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                         const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                         float* __restrict__ dqacc, const float* __restrict__ L2,
+                         const float* __restrict__ Dp, int npad, __nv_bfloat16* __restrict__ dk,
+                         __nv_bfloat16* __restrict__ dv, int64_t ld, int N, const int32_t* __restrict__ tcounts,
+                         const int32_t* __restrict__ tidx, int nb, uint32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the swizzled tiles need it; never seen, but checked
+    if (threadIdx.x == 0) flag_error(status, PRISM_DEV_TMEM);
+    return;
+  }
+  FusedSmem& sm = *reinterpret_cast<FusedSmem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x;
+  const int h = item / nb, j = item - h * nb;
+  int cnt = tcounts[item];
+  if (cnt < 0 || cnt > nb) cnt = cnt < 0 ? 0 : nb;
+  const int32_t* lst = tidx + (size_t)item * nb;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.kv_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&sm.qdo_full[s]), 1);
+      mbar_init(smem_u32(&sm.qdo_empty[s]), 1);
+      mbar_init(smem_u32(&sm.s_full[s]), 1);
+      mbar_init(smem_u32(&sm.dp_full[s]), 1);
+      mbar_init(smem_u32(&sm.p_full[s]), 4);
+      mbar_init(smem_u32(&sm.ds_full[s]), 4);
+      mbar_init(smem_u32(&sm.v_done[s]), 1);
+      mbar_init(smem_u32(&sm.k_done[s]), 1);
+      mbar_init(smem_u32(&sm.dq_full[s]), 1);
+      mbar_init(smem_u32(&sm.dq_free[s]), 4);
+    }
+    mbar_init(smem_u32(&sm.acc_done), 1);
+    mbar_init(smem_u32(&sm.in_done), 1);
+    sm.abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort = &sm.abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && cnt > 0) {
+      const uint32_t kvb = smem_u32(&sm.kv_full);
+      mbar_arrive_expect_tx(kvb, 2 * kTile);
+      tma_load_2d(smem_u32(sm.k), &tmk, h * kD, j * kB, kvb);
+      tma_load_2d(smem_u32(sm.k) + kHalf, &tmk, h * kD + 64, j * kB, kvb);
+      tma_load_2d(smem_u32(sm.v), &tmv, h * kD, j * kB, kvb);
+      tma_load_2d(smem_u32(sm.v) + kHalf, &tmv, h * kD + 64, j * kB, kvb);
+      int armed[2] = {0, 0};
+      for (int it = 0; it < cnt; ++it) {
+        const int s = it & 1;
+        if (it >= 2 && !mbar_wait(smem_u32(&sm.qdo_empty[s]), ((it >> 1) - 1) & 1, abort, status)) break;
+        int i = lst[it];
+        if (i < 0 || i >= nb) i = 0;  // lists come from the library's own transpose: never taken
+        QdoStage& g = sm.st[s];
+        const uint32_t bar = smem_u32(&sm.qdo_full[s]);
+        mbar_arrive_expect_tx(bar, 2 * kTile + 2 * kB * 4);
+        tma_load_2d(smem_u32(g.q), &tmq, h * kD, i * kB, bar);
+        tma_load_2d(smem_u32(g.q) + kHalf, &tmq, h * kD + 64, i * kB, bar);
+        tma_load_2d(smem_u32(g.dO), &tmdo, h * kD, i * kB, bar);
+        tma_load_2d(smem_u32(g.dO) + kHalf, &tmdo, h * kD + 64, i * kB, bar);
+        bulk_load(smem_u32(sm.l2[s]), L2 + (size_t)h * npad + (size_t)i * kB, kB * 4, bar);
+        bulk_load(smem_u32(sm.dr[s]), Dp + (size_t)h * npad + (size_t)i * kB, kB * 4, bar);
+        ++armed[s];
+      }
+      if (*abort) {
+        drain_wait(kvb, 0);
+        for (int s = 0; s < 2; ++s)
+          if (armed[s]) drain_wait(smem_u32(&sm.qdo_full[s]), (armed[s] - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ issuer of S^T and dP^T
+    if (lane == 0 && cnt > 0) {
+      constexpr uint32_t id_h = idesc_bf16_f32(kB, 64, false, false);  // M = 128 keys, N = 64 queries
+      const uint64_t dk_k = smem_desc(smem_u32(sm.k), 16, 1024, kSwizzle128B);
+      const uint64_t dk_v = smem_desc(smem_u32(sm.v), 16, 1024, kSwizzle128B);
+      const uint64_t dq0 = smem_desc(smem_u32(sm.st[0].q), 16, 1024, kSwizzle128B);
+      const uint64_t ddo0 = smem_desc(smem_u32(sm.st[0].dO), 16, 1024, kSwizzle128B);
+      auto koff = [](int kk) -> uint32_t { return (kk >> 2) * kHalf + (kk & 3) * 32; };
+      bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, abort, status);
+      for (int it = 0; ok && it < cnt; ++it) {
+        const int s = it & 1;
+        if (!(ok = mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status))) break;
+        const uint32_t so = s * (uint32_t)sizeof(QdoStage);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          // S^T_x overwrites the P^T_x / dS^T_x that the previous pair's dV / dK read
+          if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.v_done[x]), (it - 1) & 1, abort, status) &&
+                               mbar_wait(smem_u32(&sm.k_done[x]), (it - 1) & 1, abort, status)))
+            break;
+          tc_fence_after();
+          // the half's rows of the Q / dO tiles start 64 rows (8 KB) into each box
+          const uint64_t dq = desc_at(dq0, so + x * 8192);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + x * 64, desc_at(dk_k, koff(kk)), desc_at(dq, koff(kk)), id_h, kk > 0);
+          tc_commit(smem_u32(&sm.s_full[x]));
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          // dP^T_x overwrites the dQ^T_x of the previous pair once the drain has loaded it
+          if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.dq_free[x]), (it - 1) & 1, abort, status))) break;
+          tc_fence_after();
+          const uint64_t ddo = desc_at(ddo0, so + x * 8192);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + 128 + x * 64, desc_at(dk_v, koff(kk)), desc_at(ddo, koff(kk)), id_h, kk > 0);
+          tc_commit(smem_u32(&sm.dp_full[x]));
+        }
+      }
+      tc_commit(smem_u32(&sm.in_done));
+      drain_wait(smem_u32(&sm.in_done), 0);
+    }
+  } else if (warp == 2) {
+    // -------------------------------------------- issuer of dV, dK and dQ^T
+    if (lane == 0 && cnt > 0) {
+      constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
+      constexpr uint32_t id_dq = idesc_bf16_f32(kD, 64, true, true);  // M = 128 channels, N = 64 queries
+      const uint64_t dqmn0 = smem_desc(smem_u32(sm.st[0].q), kHalf, 1024, kSwizzle128B);
+      const uint64_t ddomn0 = smem_desc(smem_u32(sm.st[0].dO), kHalf, 1024, kSwizzle128B);
+      // K_j read as K_j^T: M = channels (two 64-wide atoms kHalf apart), K = keys
+      const uint64_t dkt = smem_desc(smem_u32(sm.k), kHalf, 1024, kSwizzle128B);
+      // dS^T_x: N = 64 queries (one atom), K = keys
+      const uint64_t dds0 = smem_desc(smem_u32(sm.ds[0]), kHalf, 1024, kSwizzle128B);
+      bool ok = true;
+      for (int it = 0; ok && it < cnt; ++it) {
+        const int s = it & 1;
+        const uint32_t so = s * (uint32_t)sizeof(QdoStage);
+        const uint64_t dqmn = desc_at(dqmn0, so), ddomn = desc_at(ddomn0, so);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (!(ok = mbar_wait(smem_u32(&sm.p_full[x]), it & 1, abort, status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // dV += P^T_x dO_x
+            mma_ts(tmem + 256, tmem + x * 64 + kk * 8, desc_at(ddomn, (x * 4 + kk) * 2048), id_ts,
+                   (it > 0 || x > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&sm.v_done[x]));
+          if (!(ok = mbar_wait(smem_u32(&sm.ds_full[x]), it & 1, abort, status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // dK += dS^T_x Q_x
+            mma_ts(tmem + 384, tmem + x * 64 + 32 + kk * 8, desc_at(dqmn, (x * 4 + kk) * 2048), id_ts,
+                   (it > 0 || x > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&sm.k_done[x]));
+          const uint64_t dds = desc_at(dds0, x * kHalf);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dQ_x^T = K_j^T dS_x^T
+            mma_ss(tmem + 128 + x * 64, desc_at(dkt, kk * 2048), desc_at(dds, kk * 2048), id_dq, kk > 0);
+          tc_commit(smem_u32(&sm.dq_full[x]));
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&sm.qdo_empty[s]));
+      }
+      // every product has completed once this barrier flips
+      tc_commit(smem_u32(&sm.acc_done));
+      drain_wait(smem_u32(&sm.acc_done), 0);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ----------------------------------------------------- softmax gradient
+    const int x = (warp - 4) >> 2;      // query half
+    const int quarter = warp & 3;
+    const int c = quarter * 32 + lane;  // key row of block j = TMEM lane
+    const int q0 = x * 64;              // this thread's query columns q0 .. q0 + 63
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const bool key_ok = j * kB + c < N;  // rows past the last token (zero-filled) give nothing
+    const uint32_t dsrow = smem_u32(sm.ds[x]) + c * 128;
+    const uint32_t sw = c & 7;
+    const f2 scale2 = f2_make(kSl2, kSl2);
+    bool ok = true;
+    for (int it = 0; it < cnt; ++it) {
+      const int s = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status) &&
+                                       mbar_wait(smem_u32(&sm.s_full[x]), it & 1, abort, status));
+      if (!ok) break;
+      tc_fence_after();
+      const float4* l2v = reinterpret_cast<const float4*>(sm.l2[s] + q0);
+      const float4* drv = reinterpret_cast<const float4*>(sm.dr[s] + q0);
+      f2 p[32];  // P^T of this key row and the half's 64 query columns, fp32 pairs
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {  // 16 query columns at a time
+        uint32_t sr[16];
+        tmem_ld16(lane_base + x * 64 + cc * 16, sr);
+        tmem_wait_ld();
+        reg_fence16(sr);
+        uint32_t pp[8];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 L = l2v[cc * 4 + q4];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int e = 4 * q4 + 2 * u;
+            const f2 nl = u ? f2_make(-L.z, -L.w) : f2_make(-L.x, -L.y);
+            float a0, a1;
+            f2_split(f2_fma(f2_make(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), scale2, nl), a0, a1);
+            const f2 pv = key_ok ? f2_make(fast_exp2(a0), fast_exp2(a1)) : f2_make(0.f, 0.f);
+            p[cc * 8 + 2 * q4 + u] = pv;
+            pp[2 * q4 + u] = f2_pack_bf16(pv);
+          }
+        }
+        // P^T_x over columns 8cc .. 8cc + 7 of S^T_x (already loaded above)
+        tmem_st8(lane_base + x * 64 + cc * 8, pp);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[x]));
+      // dS^T_x overwrites the shared tile that the previous pair's dQ^T read
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dp_full[x]), it & 1, abort, status) &&
+                                       (it == 0 || mbar_wait(smem_u32(&sm.dq_full[x]), (it - 1) & 1, abort, status)));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t pr[16];
+        tmem_ld16(lane_base + 128 + x * 64 + cc * 16, pr);
+        tmem_wait_ld();
+        reg_fence16(pr);
+        uint32_t dd[8];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 Dv = drv[cc * 4 + q4];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int e = 4 * q4 + 2 * u;
+            const f2 nd = u ? f2_make(-Dv.z, -Dv.w) : f2_make(-Dv.x, -Dv.y);
+            dd[2 * q4 + u] = f2_pack_bf16(
+                f2_mul(p[cc * 8 + 2 * q4 + u], f2_add(f2_make(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])), nd)));
+          }
+        }
+        // dS^T_x over columns 32 + 8cc .. of S^T_x (A of dK) and into row c of the
+        // shared dS^T_x tile (B of dQ^T): 16-byte chunk k of the row at k ^ (c & 7)
+        tmem_st8(lane_base + x * 64 + 32 + cc * 8, dd);
+        st_shared_v4(dsrow + ((((uint32_t)(2 * cc)) ^ sw) << 4), dd[0], dd[1], dd[2], dd[3]);
+        st_shared_v4(dsrow + ((((uint32_t)(2 * cc + 1)) ^ sw) << 4), dd[4], dd[5], dd[6], dd[7]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.ds_full[x]));
+    }
+    const int col = j * kB + c;
+    __nv_bfloat16* dk_row = dk + (int64_t)col * ld + (int64_t)h * kD + q0;
+    __nv_bfloat16* dv_row = dv + (int64_t)col * ld + (int64_t)h * kD + q0;
+    if (ok && cnt > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_done), 0, abort, status));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {  // dV, then dK (scaled by 1/sqrt(d))
+          __nv_bfloat16* out = which ? dk_row : dv_row;
+          const float sc = which ? kScale : 1.f;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t rr[32];
+            tmem_load_row32(lane_base + 256 + which * 128 + q0 + c2 * 32, rr);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * sc, __uint_as_float(rr[2 * e + 1]) * sc);
+            if (col < N) {
+              uint4* dst = reinterpret_cast<uint4*>(out + c2 * 32);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            }
+          }
+        }
+      }
+    } else if (cnt == 0 && col < N) {
+      uint4* a = reinterpret_cast<uint4*>(dk_row);
+      uint4* b = reinterpret_cast<uint4*>(dv_row);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[e] = b[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  } else if (warp >= 12) {
+    // -------------------------------------------------------------- dQ drain
+    // Thread = channel dch (TMEM lane of dQ^T).  Per query half: load the 64 query
+    // columns, free the TMEM columns, then per 4 queries transpose 4 x 4 values inside
+    // each quad of lanes (after it, lane 4g + k holds query 4s + k of channels 4g ..
+    // 4g + 3) and add them to the accumulator with 16-byte reductions: one warp
+    // instruction covers 4 query rows x 128 contiguous bytes.
+    const int quarter = warp & 3;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int k = lane & 3, g = lane >> 2;
+    const int64_t acc_ld = (int64_t)gridDim.x / nb * kD;  // Hh * d
+    bool ok = true;
+    for (int it = 0; ok && it < cnt; ++it) {
+      int i = lst[it];
+      if (i < 0 || i >= nb) i = 0;
+#pragma unroll 1
+      for (int x = 0; x < 2; ++x) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full[x]), it & 1, abort, status));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld32(lane_base + 128 + x * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(lane_base + 128 + x * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_wait_ld();
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free[x]));
+        float* base = dqacc + (int64_t)(i * kB + x * 64 + k) * acc_ld + (int64_t)h * kD + quarter * 32 + 4 * g;
+#pragma unroll
+        for (int s4 = 0; s4 < 16; ++s4) {
+          float v0 = __uint_as_float(r[4 * s4]), v1 = __uint_as_float(r[4 * s4 + 1]);
+          float v2 = __uint_as_float(r[4 * s4 + 2]), v3 = __uint_as_float(r[4 * s4 + 3]);
+          // swap the off-diagonal 2 x 2 blocks with lane k ^ 2, then transpose inside them with k ^ 1
+          {
+            const bool hi = k & 2;
+            const float a = __shfl_xor_sync(0xffffffffu, hi ? v0 : v2, 2);
+            const float b = __shfl_xor_sync(0xffffffffu, hi ? v1 : v3, 2);
+            if (hi) v0 = a, v1 = b;
+            else v2 = a, v3 = b;
+          }
+          {
+            const bool odd = k & 1;
+            const float a = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+            const float b = __shfl_xor_sync(0xffffffffu, odd ? v2 : v3, 1);
+            if (odd) v0 = a, v2 = b;
+            else v1 = a, v3 = b;
+          }
+          red_add_v4(base + (int64_t)(4 * s4) * acc_ld, v0, v1, v2, v3);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// dq[r][h][c] = bf16(acc[r][h * d + c] / sqrt(d)): one thread per 8 channels of a token row.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, int Hh, int N,
+                                                         __nv_bfloat16* __restrict__ dq, int64_t ld) {
+  const int64_t per_row = (int64_t)Hh * (kD / 8);
+  const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= (int64_t)N * per_row) return;
+  const int64_t r = v / per_row;
+  const int cv = (int)(v - r * per_row);
+  const float4* src = reinterpret_cast<const float4*>(acc + r * Hh * kD + (int64_t)cv * 8);
+  const float4 a = __ldcs(src), b = __ldcs(src + 1);
+  uint4 o;
+  o.x = pack_bf16x2(a.x * kScale, a.y * kScale);
+  o.y = pack_bf16x2(a.z * kScale, a.w * kScale);
+  o.z = pack_bf16x2(b.x * kScale, b.y * kScale);
+  o.w = pack_bf16x2(b.z * kScale, b.w * kScale);
+  *reinterpret_cast<uint4*>(dq + r * ld + (int64_t)cv * 8) = o;
+}
+
 }  // namespace
 
 size_t bwd_tc_rowstats_bytes(int Hh, int nb) { return (size_t)2 * Hh * nb * kB * sizeof(float); }
+size_t bwd_tc_dqacc_bytes(int Hh, int nb) { return (size_t)nb * kB * Hh * kD * sizeof(float); }
 
 cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,
                               const int32_t* idx, int nb, void* dq, void* dk, void* dv, const int32_t* tcounts,
-                              const int32_t* tidx, float* rowstats, cudaStream_t st, uint32_t* status) {
+                              const int32_t* tidx, float* rowstats, float* dqacc, cudaStream_t st,
+                              uint32_t* status) {
   const int npad = nb * kB;
   float* L2 = rowstats;
   float* Dp = rowstats + (size_t)Hh * npad;
@@ -677,7 +1105,8 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
   {
     HookScope hs("bwd_prep", st);
     bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, ld, N, Hh, npad, L2, Dp);
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, ld, N, Hh, npad, L2, Dp,
+        dqacc);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -688,6 +1117,25 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
       !tensor_map_2d_bf16(&mv, v, inner, N, row_bytes, 64, kB) ||
       !tensor_map_2d_bf16(&mdo, dO, inner, N, row_bytes, 64, kB))
     return cudaErrorInvalidValue;
+  if (dqacc) {
+    // fused: one kernel for dK, dV and the fp32 dQ accumulator, then the conversion
+    if ((e = cudaFuncSetAttribute(bsa_bwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kFusedSmemBytes)) != cudaSuccess)
+      return e;
+    {
+      HookScope hs("bsa_bwd_tc", st);
+      bsa_bwd_fused_kernel<<<(unsigned)Hh * nb, kFusedThreads, kFusedSmemBytes, st>>>(
+          mq, mk, mv, mdo, dqacc, L2, Dp, npad, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), ld,
+          N, tcounts, tidx, nb, status);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t vecs = (int64_t)N * Hh * (kD / 8);
+    HookScope hs("dq_convert", st);
+    dq_convert_kernel<<<(unsigned)((vecs + 255) / 256), 256, 0, st>>>(dqacc, Hh, N, static_cast<__nv_bfloat16*>(dq),
+                                                                      ld);
+    return cudaGetLastError();
+  }
+  // split: dQ recomputes S and dP per query block; dK / dV per key block
   if ((e = cudaFuncSetAttribute(bsa_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)kDqSmemBytes)) != cudaSuccess)
     return e;

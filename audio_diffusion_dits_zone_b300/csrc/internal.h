@@ -39,6 +39,17 @@ cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const fl
                         const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm, void* ws, cudaStream_t st,
                         uint32_t* status);
 
+// The zone step in two halves, for channels split over several calls (one per rank):
+// per-zone, per-axis partial sums of one call's channels ([Z][3]), and the shapes and
+// permutation from partial sums gathered as [nparts][Z][3] (summed in part order).
+size_t zone_partials_ws_bytes(const ZoneGeom& g, int C);
+cudaError_t zone_partials_launch(const void* feat, int dtype, int64_t ld, int C, const ZoneGeom& g, float* out,
+                                 void* ws, cudaStream_t st, uint32_t* status);
+size_t zone_from_partials_ws_bytes(const ZoneGeom& g);
+cudaError_t zone_from_partials_launch(const float* parts, int nparts, int C_total, const float* a2v,
+                                      const ZoneGeom& g, const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm,
+                                      void* ws, cudaStream_t st);
+
 // pool_score.cu
 cudaError_t pool_launch(const void* q, const void* k, const void* v, int dtype, int64_t ld, const int32_t* perm,
                         int N, int Hh, int d, int B, void* qb, void* kb, void* vb, int64_t ldb, float* qbar,
@@ -49,6 +60,11 @@ cudaError_t scores_launch(const float* qbar, const float* kbar, int Hh, int nb, 
 // select.cu
 cudaError_t select_launch(const float* scores, int Hh, int nb, int k_top, double tau, int32_t* counts,
                           int32_t* idx, cudaStream_t st);
+
+// score_select.cu: scores and selection in one kernel (no score matrix in memory).
+bool score_select_supported(int nb, int d);
+cudaError_t score_select_launch(const float* qbar, const float* kbar, int Hh, int nb, int d, int k_top, double tau,
+                                int32_t* counts, int32_t* idx, cudaStream_t st);
 
 // bsa_simt.cu (CUDA-core attention for f32 inputs and shapes outside the tensor-core path)
 cudaError_t bsa_fwd_simt_launch(const void* q, const void* k, const void* v, int dtype, int64_t ld, int N, int Hh,
@@ -83,14 +99,29 @@ cudaError_t a2v_attn_launch(const void* qv, const void* ka, const void* va, int6
 // a2v[n] = sqrt(sum_h sqn[h][n]).
 cudaError_t a2v_reduce_launch(const float* sqn, int N, int Hh, float* a2v, cudaStream_t st);
 size_t bwd_tc_rowstats_bytes(int Hh, int nb);
+// fp32 dQ accumulator of the fused backward: [nb * 128][Hh * 128]
+size_t bwd_tc_dqacc_bytes(int Hh, int nb);
+// dqacc != NULL: the fused kernel (dK, dV and dQ in one pass over the transposed lists,
+// dQ reduce-added into dqacc, then converted); dqacc == NULL: the split kernels (dQ per
+// query block, recomputing S and dP; dK and dV per key block).
 cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,
                               const int32_t* idx, int nb, void* dq, void* dk, void* dv, const int32_t* tcounts,
-                              const int32_t* tidx, float* rowstats, cudaStream_t st, uint32_t* status);
+                              const int32_t* tidx, float* rowstats, float* dqacc, cudaStream_t st,
+                              uint32_t* status);
+
+// pab.cu: per-head mean squared difference of two [N][Hh][d] tensors (row stride ld);
+// part holds Hh * attn_mse_chunks(N, Hh) fp32 partial sums.
+int attn_mse_chunks(int N, int Hh);
+cudaError_t attn_mse_launch(const void* a, const void* b, int dtype, int64_t ld, int N, int Hh, int d, float* mse,
+                            float* part, cudaStream_t st);
 
 // Driver entry point for tensor-map encoding (resolved once through the runtime).
 bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                         uint32_t box_inner, uint32_t box_outer);
+// fp32 2D tensor map with 128-byte swizzle (box_inner * 4 <= 128 bytes).
+bool tensor_map_2d_f32_sw128(void* map_out, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                             uint32_t box_inner, uint32_t box_outer);
 // bf16 tensor map of rank 1..5, no swizzle: dims innermost first, strides_bytes[k] =
 // byte stride of dimension k + 1.
 bool tensor_map_bf16(void* map_out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,

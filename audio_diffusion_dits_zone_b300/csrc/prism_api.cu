@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -109,6 +110,18 @@ int check_attention_args(const void* q, const void* k, const void* v, int32_t dt
   return PRISM_OK;
 }
 
+// The tensor-core backward runs the fused kernel (dK, dV and dQ in one pass, dQ
+// reduce-added in fp32) unless PRISM_BWD_SPLIT=1 is set in the environment when the
+// library is first used: then the split kernels (dQ in its own pass, recomputing S
+// and dP), kept to compare the two designs.  Both compute the full gradients.
+bool split_backward() {
+  static const bool split = [] {
+    const char* v = std::getenv("PRISM_BWD_SPLIT");
+    return v && v[0] == '1';
+  }();
+  return split;
+}
+
 bool use_tc(int32_t dtype, int32_t d, int32_t B, int64_t ld, std::initializer_list<const void*> ptrs) {
   if (dtype != PRISM_BF16 || d != 128 || B != 128 || ld % 8 != 0) return false;
   for (const void* p : ptrs)
@@ -134,37 +147,95 @@ void launch_hook(const char* kernel, cudaStream_t st, int phase) {
 
 extern "C" {
 
+}  // extern "C"
+
+namespace {
+
+// Grid, zone extents and (optionally) shape set of the zone calls; PRISM_OK or an error.
+int zone_geometry(int32_t T, int32_t H, int32_t W, int32_t zt, int32_t zh, int32_t zw, prism::ZoneGeom* g) {
+  if (T < 1 || H < 1 || W < 1) return fail(PRISM_EINVAL, "grid must be positive");
+  if ((int64_t)T * H * W > INT32_MAX) return fail(PRISM_EINVAL, "too many tokens");
+  if (zt < 1 || zh < 1 || zw < 1) return fail(PRISM_EINVAL, "zone extents must be >= 1");
+  *g = prism::ZoneGeom{};
+  g->T = T, g->H = H, g->W = W, g->zt = zt, g->zh = zh, g->zw = zw;
+  g->nzt = (int)cdiv(T, zt), g->nzh = (int)cdiv(H, zh), g->nzw = (int)cdiv(W, zw);
+  g->Z = g->nzt * g->nzh * g->nzw;
+  g->max_tokens = std::min(zt, T) * std::min(zh, H) * std::min(zw, W);
+  if ((int64_t)g->max_tokens * 8 * 4 > 200 * 1024)
+    return fail(PRISM_EUNSUPPORTED, "zones of %d tokens exceed the shared-memory staging limit (6400)",
+                g->max_tokens);
+  return PRISM_OK;
+}
+
+int shape_set(const int32_t* shapes, int32_t n_shapes, prism::ShapeSet* ss) {
+  if (n_shapes < 1 || n_shapes > 8 || !shapes) return fail(PRISM_EINVAL, "need 1..8 shapes (host array)");
+  *ss = prism::ShapeSet{};
+  ss->n = n_shapes;
+  for (int s = 0; s < n_shapes; ++s)
+    for (int a = 0; a < 3; ++a) {
+      ss->e[s][a] = shapes[3 * s + a];
+      if (ss->e[s][a] < 1) return fail(PRISM_EINVAL, "shape extents must be >= 1");
+    }
+  return PRISM_OK;
+}
+
+int feature_args(int32_t feat_dtype, int64_t feat_ld, int32_t C) {
+  if (feat_dtype != PRISM_F32 && feat_dtype != PRISM_BF16) return fail(PRISM_EINVAL, "feat_dtype invalid");
+  if (C < 1 || feat_ld < C) return fail(PRISM_EINVAL, "need 1 <= C <= feat_ld");
+  return PRISM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int prism_zone_shapes(const void* feat, int32_t feat_dtype, int64_t feat_ld, int32_t C, const float* a2v, int32_t T,
                       int32_t H, int32_t W, int32_t zt, int32_t zh, int32_t zw, const int32_t* shapes,
                       int32_t n_shapes, int32_t* zone_shape, int32_t* perm, void* ws, size_t* ws_bytes,
                       void* stream) {
-  if (feat_dtype != PRISM_F32 && feat_dtype != PRISM_BF16) return fail(PRISM_EINVAL, "feat_dtype invalid");
-  if (T < 1 || H < 1 || W < 1) return fail(PRISM_EINVAL, "grid must be positive");
-  if ((int64_t)T * H * W > INT32_MAX) return fail(PRISM_EINVAL, "too many tokens");
-  if (zt < 1 || zh < 1 || zw < 1) return fail(PRISM_EINVAL, "zone extents must be >= 1");
-  if (C < 1 || feat_ld < C) return fail(PRISM_EINVAL, "need 1 <= C <= feat_ld");
-  if (n_shapes < 1 || n_shapes > 8 || !shapes) return fail(PRISM_EINVAL, "need 1..8 shapes (host array)");
-  prism::ShapeSet ss{};
-  ss.n = n_shapes;
-  for (int s = 0; s < n_shapes; ++s)
-    for (int a = 0; a < 3; ++a) {
-      ss.e[s][a] = shapes[3 * s + a];
-      if (ss.e[s][a] < 1) return fail(PRISM_EINVAL, "shape extents must be >= 1");
-    }
-  prism::ZoneGeom g{};
-  g.T = T, g.H = H, g.W = W, g.zt = zt, g.zh = zh, g.zw = zw;
-  g.nzt = (int)cdiv(T, zt), g.nzh = (int)cdiv(H, zh), g.nzw = (int)cdiv(W, zw);
-  g.Z = g.nzt * g.nzh * g.nzw;
-  g.max_tokens = std::min(zt, T) * std::min(zh, H) * std::min(zw, W);
-  if ((int64_t)g.max_tokens * 8 * 4 > 200 * 1024)
-    return fail(PRISM_EUNSUPPORTED, "zones of %d tokens exceed the shared-memory staging limit (6400)",
-                g.max_tokens);
+  prism::ZoneGeom g;
+  prism::ShapeSet ss;
   int rc;
+  if ((rc = feature_args(feat_dtype, feat_ld, C)) != PRISM_OK) return rc;
+  if ((rc = shape_set(shapes, n_shapes, &ss)) != PRISM_OK) return rc;
+  if ((rc = zone_geometry(T, H, W, zt, zh, zw, &g)) != PRISM_OK) return rc;
   if (ws_query(ws, ws_bytes, ws_round(prism::zone_ws_bytes(g, C, feat_dtype)), &rc)) return rc;
   if (!feat || !a2v || !zone_shape || !perm) return fail(PRISM_EINVAL, "NULL pointer");
   cudaError_t e = prism::zone_launch(feat, feat_dtype, feat_ld, C, a2v, g, ss, zone_shape, perm, ws,
                                      static_cast<cudaStream_t>(stream), status_ptr());
   return e == cudaSuccess ? (launched(4), ok()) : cuda_fail(e, "prism_zone_shapes");
+}
+
+int prism_zone_partials(const void* feat, int32_t feat_dtype, int64_t feat_ld, int32_t C, int32_t T, int32_t H,
+                        int32_t W, int32_t zt, int32_t zh, int32_t zw, float* partials, void* ws, size_t* ws_bytes,
+                        void* stream) {
+  prism::ZoneGeom g;
+  int rc;
+  if ((rc = feature_args(feat_dtype, feat_ld, C)) != PRISM_OK) return rc;
+  if ((rc = zone_geometry(T, H, W, zt, zh, zw, &g)) != PRISM_OK) return rc;
+  if (ws_query(ws, ws_bytes, ws_round(prism::zone_partials_ws_bytes(g, C)), &rc)) return rc;
+  if (!feat || !partials) return fail(PRISM_EINVAL, "NULL pointer");
+  cudaError_t e = prism::zone_partials_launch(feat, feat_dtype, feat_ld, C, g, partials, ws,
+                                              static_cast<cudaStream_t>(stream), status_ptr());
+  return e == cudaSuccess ? (launched(2), ok()) : cuda_fail(e, "prism_zone_partials");
+}
+
+int prism_zone_shapes_from_partials(const float* partials, int32_t n_parts, int32_t C_total, const float* a2v,
+                                    int32_t T, int32_t H, int32_t W, int32_t zt, int32_t zh, int32_t zw,
+                                    const int32_t* shapes, int32_t n_shapes, int32_t* zone_shape, int32_t* perm,
+                                    void* ws, size_t* ws_bytes, void* stream) {
+  prism::ZoneGeom g;
+  prism::ShapeSet ss;
+  int rc;
+  if (n_parts < 1 || n_parts > 4096) return fail(PRISM_EINVAL, "n_parts must be in [1, 4096]");
+  if (C_total < 1) return fail(PRISM_EINVAL, "C_total must be >= 1");
+  if ((rc = shape_set(shapes, n_shapes, &ss)) != PRISM_OK) return rc;
+  if ((rc = zone_geometry(T, H, W, zt, zh, zw, &g)) != PRISM_OK) return rc;
+  if (ws_query(ws, ws_bytes, ws_round(prism::zone_from_partials_ws_bytes(g)), &rc)) return rc;
+  if (!partials || !a2v || !zone_shape || !perm) return fail(PRISM_EINVAL, "NULL pointer");
+  cudaError_t e = prism::zone_from_partials_launch(partials, n_parts, C_total, a2v, g, ss, zone_shape, perm, ws,
+                                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? (launched(3), ok()) : cuda_fail(e, "prism_zone_shapes_from_partials");
 }
 
 int prism_pool_score(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld, const int32_t* perm,
@@ -204,6 +275,23 @@ int prism_select(const float* scores, int32_t Hh, int32_t nb, double sparsity, d
   cudaError_t e = prism::select_launch(scores, Hh, nb, k_top, cdf_tau, counts, idx,
                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? (launched(1), ok()) : cuda_fail(e, "prism_select");
+}
+
+int prism_score_select(const float* qbar, const float* kbar, int32_t Hh, int32_t nb, int32_t d, double sparsity,
+                       double cdf_tau, int32_t* counts, int32_t* idx, void* stream) {
+  if (!qbar || !kbar || !counts || !idx) return fail(PRISM_EINVAL, "NULL pointer");
+  if (Hh < 1 || nb < 1 || d < 1) return fail(PRISM_EINVAL, "Hh, nb and d must be >= 1");
+  if (!(sparsity >= 0.0 && sparsity < 1.0)) return fail(PRISM_EINVAL, "sparsity must be in [0, 1)");
+  if (!(cdf_tau >= 0.0 && cdf_tau <= 1.0)) return fail(PRISM_EINVAL, "cdf_tau must be in [0, 1]");
+  if (!prism::score_select_supported(nb, d))
+    return fail(PRISM_EUNSUPPORTED, "prism_score_select needs d a multiple of 8, d <= 256, nb <= 4096 (got d = %d, "
+                                    "nb = %d); use prism_pool_score scores + prism_select", d, nb);
+  if (!aligned16(qbar) || !aligned16(kbar)) return fail(PRISM_EINVAL, "qbar and kbar must be 16-byte aligned");
+  const double kk = std::ceil((1.0 - sparsity) * nb - 1e-9);
+  const int k_top = (int)std::min<double>(nb, std::max<double>(1.0, kk));
+  cudaError_t e = prism::score_select_launch(qbar, kbar, Hh, nb, d, k_top, cdf_tau, counts, idx,
+                                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? (launched(1), ok()) : cuda_fail(e, "prism_score_select");
 }
 
 int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32_t dtype, int64_t ld, int32_t N,
@@ -249,25 +337,43 @@ int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk, const
                   size_t* ws_bytes, void* stream) {
   int rc = check_attention_args(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb);
   if (rc != PRISM_OK) return rc;
-  const size_t lists = prism::lists_ws_bytes(Hh, nb);
+  // workspace: transposed lists | row statistics | (fused tensor-core path) fp32 dQ accumulator
+  auto r256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t lists = r256(prism::lists_ws_bytes(Hh, nb));
   const bool tc = use_tc(dtype, d, B, ld, {q_blk, k_blk, v_blk, o_blk, do_blk, dq, dk, dv});
-  const size_t rows = tc ? prism::bwd_tc_rowstats_bytes(Hh, nb) : (size_t)Hh * N * sizeof(float);
-  if (ws_query(ws, ws_bytes, ws_round(lists + ((rows + 255) & ~(size_t)255)), &rc)) return rc;
+  const bool fused = tc && !split_backward();
+  const size_t rows = r256(tc ? prism::bwd_tc_rowstats_bytes(Hh, nb) : (size_t)Hh * N * sizeof(float));
+  const size_t acc = fused ? prism::bwd_tc_dqacc_bytes(Hh, nb) : 0;
+  if (ws_query(ws, ws_bytes, ws_round(lists + rows + acc), &rc)) return rc;
   if (!o_blk || !do_blk || !lse || !dq || !dk || !dv) return fail(PRISM_EINVAL, "NULL pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* tcounts = nullptr;
   int32_t* tidx = nullptr;
   float* rowstats = reinterpret_cast<float*>(static_cast<char*>(ws) + lists);
+  float* dqacc = fused ? reinterpret_cast<float*>(static_cast<char*>(ws) + lists + rows) : nullptr;
   cudaError_t e = prism::transpose_lists_launch(counts, idx, Hh, nb, ws, &tcounts, &tidx, st, status_ptr());
   if (e == cudaSuccess) {
     if (tc)
       e = prism::bsa_bwd_tc_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, ld, N, Hh, counts, idx, nb, dq, dk, dv,
-                                   tcounts, tidx, rowstats, st, status_ptr());
+                                   tcounts, tidx, rowstats, dqacc, st, status_ptr());
     else
       e = prism::bsa_bwd_simt_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, dtype, ld, N, Hh, d, B, counts, idx,
                                      nb, dq, dk, dv, tcounts, tidx, rowstats, st, status_ptr());
   }
   return e == cudaSuccess ? (launched(5), ok()) : cuda_fail(e, "prism_bsa_bwd");
+}
+
+int prism_attn_mse(const void* a, const void* b, int32_t dtype, int64_t ld, int32_t N, int32_t Hh, int32_t d,
+                   float* mse, void* ws, size_t* ws_bytes, void* stream) {
+  if (dtype != PRISM_F32 && dtype != PRISM_BF16) return fail(PRISM_EINVAL, "dtype must be PRISM_F32 or PRISM_BF16");
+  if (N < 1 || Hh < 1 || d < 1) return fail(PRISM_EINVAL, "N, Hh and d must be >= 1");
+  if (ld < (int64_t)Hh * d) return fail(PRISM_EINVAL, "ld = %lld < Hh * d = %d", (long long)ld, Hh * d);
+  int rc;
+  if (ws_query(ws, ws_bytes, ws_round((size_t)Hh * prism::attn_mse_chunks(N, Hh) * sizeof(float)), &rc)) return rc;
+  if (!a || !b || !mse) return fail(PRISM_EINVAL, "NULL pointer");
+  cudaError_t e = prism::attn_mse_launch(a, b, dtype, ld, N, Hh, d, mse, static_cast<float*>(ws),
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? (launched(2), ok()) : cuda_fail(e, "prism_attn_mse");
 }
 
 int prism_status_check(void* stream, uint32_t* word) {

@@ -436,10 +436,13 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1)
       drain_wait(smem_u32(&sm.full[warp][s & 1]), (s >> 1) & 1);
 }
 
-// stats[z * 8 + {0,1,2}] = v_a, {3,4,5} = u_a, 6 = zone mean of a2v.
-__global__ void __launch_bounds__(kZoneThreads) zone_finalize_kernel(const float* __restrict__ part, int nchunks,
-                                                                     const float* __restrict__ a2v, ZoneGeom g,
-                                                                     int C, float* __restrict__ stats) {
+// stats[z * 8 + {0,1,2}] = v_a, {3,4,5} = u_a, 6 = zone mean of a2v.  The video term is
+// the sum, in order c = 0 .. nparts - 1, of the partial sums part[z * zs + c * cs + a]
+// (per-chunk partials of one call: zs = nparts * 3, cs = 3; partials of several
+// channel slices gathered as [nparts][Z][3]: zs = 3, cs = Z * 3), over C channels.
+__global__ void __launch_bounds__(kZoneThreads) zone_finalize_kernel(const float* __restrict__ part, int nparts,
+                                                                     int zs, int cs, const float* __restrict__ a2v,
+                                                                     ZoneGeom g, int C, float* __restrict__ stats) {
   extern __shared__ float as[];  // zone's a2v values
   __shared__ float red[(kZoneThreads / 32) * 3 + 3];
   const int z = blockIdx.x;
@@ -478,13 +481,23 @@ __global__ void __launch_bounds__(kZoneThreads) zone_finalize_kernel(const float
     const float inv_tok = 1.f / (float)ntok;
     for (int a = 0; a < 3; ++a) {
       float s = 0.f;
-      for (int c = 0; c < nchunks; ++c) s += part[((size_t)z * nchunks + c) * 3 + a];
+      for (int c = 0; c < nparts; ++c) s += part[(size_t)z * zs + (size_t)c * cs + a];
       stats[z * 8 + a] = s / ((float)C * (float)ntok);
       stats[z * 8 + 3 + a] = u[a] * inv_tok;
     }
     stats[z * 8 + 6] = m[0] * inv_tok;
     stats[z * 8 + 7] = 0.f;
   }
+}
+
+// out[z][a] = sum over chunks c (in order) of part[z][c][a].
+__global__ void zone_sum_chunks_kernel(const float* __restrict__ part, int nchunks, int Z, float* __restrict__ out) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= Z * 3) return;
+  const int z = t / 3, a = t - z * 3;
+  float s = 0.f;
+  for (int c = 0; c < nchunks; ++c) s += part[((size_t)z * nchunks + c) * 3 + a];
+  out[t] = s;
 }
 
 __global__ void __launch_bounds__(1024) zone_choose_kernel(const float* __restrict__ stats, int Z, ShapeSet shapes,
@@ -587,16 +600,18 @@ size_t zone_ws_bytes(const ZoneGeom& g, int C, int /*dtype*/) {
   return align256((size_t)g.Z * nchunks * 3 * sizeof(float)) + align256((size_t)g.Z * 8 * sizeof(float));
 }
 
-cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const float* a2v, const ZoneGeom& g,
-                        const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm, void* ws, cudaStream_t st,
-                        uint32_t* status) {
+namespace {
+
+// Per-zone, per-axis partial sums of one call's feature channels, per channel chunk:
+// part[z][chunk][a] = sum over the chunk's channels and the zone's lines along axis a
+// of the squared deviations from the line mean.  *nchunks_out receives the chunks.
+cudaError_t zone_partials_stage(const void* feat, int dtype, int64_t ld, int C, const ZoneGeom& g, float* part,
+                                int* nchunks_out, cudaStream_t st, uint32_t* status) {
   const int ch = chunk_channels(g);
   const int variant = lines_variant(g, C, ld, dtype, feat);
   const bool by64 = variant || tma_variant(g, C, ld, dtype, feat);
   const int nchunks = by64 ? (C + kLinesChannels - 1) / kLinesChannels : (C + ch - 1) / ch;
-  const int ws_chunks = std::max((C + ch - 1) / ch, (C + kLinesChannels - 1) / kLinesChannels);
-  float* part = reinterpret_cast<float*>(ws);
-  float* stats = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)g.Z * ws_chunks * 3 * 4));
+  *nchunks_out = nchunks;
   const size_t smem = (size_t)g.max_tokens * ch * sizeof(float);
   const dim3 grid(g.Z, nchunks);
   cudaError_t e;
@@ -671,11 +686,18 @@ cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const fl
       k<<<grid, kZoneThreads, smem, st>>>(static_cast<const float*>(feat), ld, C, g, ch, part);
     }
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// stats, zone shapes and the permutation from partial sums part (strides zs, cs).
+cudaError_t zone_choose_stage(const float* part, int nparts, int zs, int cs, int C, const float* a2v,
+                              const ZoneGeom& g, const ShapeSet& shapes, float* stats, int32_t* zone_shape,
+                              int32_t* perm, cudaStream_t st) {
+  cudaError_t e;
   {
-  HookScope hs("zone_finalize", st);
-  zone_finalize_kernel<<<g.Z, kZoneThreads, (size_t)g.max_tokens * sizeof(float), st>>>(part, nchunks, a2v, g, C,
-                                                                                        stats);
+    HookScope hs("zone_finalize", st);
+    zone_finalize_kernel<<<g.Z, kZoneThreads, (size_t)g.max_tokens * sizeof(float), st>>>(part, nparts, zs, cs, a2v,
+                                                                                          g, C, stats);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
@@ -690,6 +712,49 @@ cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const fl
     zone_perm_kernel<<<blocks, 256, 0, st>>>(g, zone_shape, shapes, perm);
   }
   return cudaGetLastError();
+}
+
+int ws_chunks_of(const ZoneGeom& g, int C) {
+  const int ch = chunk_channels(g);
+  return std::max((C + ch - 1) / ch, (C + kLinesChannels - 1) / kLinesChannels);
+}
+
+}  // namespace
+
+cudaError_t zone_launch(const void* feat, int dtype, int64_t ld, int C, const float* a2v, const ZoneGeom& g,
+                        const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm, void* ws, cudaStream_t st,
+                        uint32_t* status) {
+  float* part = reinterpret_cast<float*>(ws);
+  float* stats =
+      reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)g.Z * ws_chunks_of(g, C) * 3 * 4));
+  int nchunks = 0;
+  cudaError_t e = zone_partials_stage(feat, dtype, ld, C, g, part, &nchunks, st, status);
+  if (e != cudaSuccess) return e;
+  return zone_choose_stage(part, nchunks, nchunks * 3, 3, C, a2v, g, shapes, stats, zone_shape, perm, st);
+}
+
+size_t zone_partials_ws_bytes(const ZoneGeom& g, int C) {
+  return align256((size_t)g.Z * ws_chunks_of(g, C) * 3 * sizeof(float));
+}
+
+cudaError_t zone_partials_launch(const void* feat, int dtype, int64_t ld, int C, const ZoneGeom& g, float* out,
+                                 void* ws, cudaStream_t st, uint32_t* status) {
+  float* part = reinterpret_cast<float*>(ws);
+  int nchunks = 0;
+  cudaError_t e = zone_partials_stage(feat, dtype, ld, C, g, part, &nchunks, st, status);
+  if (e != cudaSuccess) return e;
+  HookScope hs("zone_sum_chunks", st);
+  zone_sum_chunks_kernel<<<(g.Z * 3 + 255) / 256, 256, 0, st>>>(part, nchunks, g.Z, out);
+  return cudaGetLastError();
+}
+
+size_t zone_from_partials_ws_bytes(const ZoneGeom& g) { return align256((size_t)g.Z * 8 * sizeof(float)); }
+
+cudaError_t zone_from_partials_launch(const float* parts, int nparts, int C_total, const float* a2v,
+                                      const ZoneGeom& g, const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm,
+                                      void* ws, cudaStream_t st) {
+  return zone_choose_stage(parts, nparts, 3, g.Z * 3, C_total, a2v, g, shapes, static_cast<float*>(ws), zone_shape,
+                           perm, st);
 }
 
 }  // namespace prism

@@ -15,8 +15,12 @@ from . import synth
 class PrismLayer:
     """Device-resident state of one attention layer for a ``synth.Workload``."""
 
-    def __init__(self, wl: synth.Workload, device="cuda", sparsity=None, train=None):
+    def __init__(self, wl: synth.Workload, device="cuda", sparsity=None, train=None, fused_select=False):
+        """fused_select: block scores and selection in one call (prism_score_select), the
+        score matrix never written; otherwise prism_pool_score writes the scores and
+        prism_select reads them."""
         self.wl = wl
+        self.fused_select = fused_select
         self.device = torch.device(device)
         self.sparsity = wl.sparsity if sparsity is None else sparsity
         self.train = (wl.mode == "fwd+bwd") if train is None else train
@@ -37,7 +41,7 @@ class PrismLayer:
         self.v_blk = torch.empty_like(self.v)
         self.qbar = torch.empty(Hh, nb, d, dtype=torch.float32, **e)
         self.kbar = torch.empty(Hh, nb, d, dtype=torch.float32, **e)
-        self.scores = torch.empty(Hh, nb, nb, dtype=torch.float32, **e)
+        self.scores = None if fused_select else torch.empty(Hh, nb, nb, dtype=torch.float32, **e)
         self.counts = torch.empty(Hh, nb, dtype=torch.int32, **e)
         self.idx = torch.empty(Hh, nb, nb, dtype=torch.int32, **e)
         self.o_blk = torch.empty_like(self.q)
@@ -75,8 +79,17 @@ class PrismLayer:
         P.prism_pool_score(self.q, self.k, self.v, self.perm, self.wl.block, self.q_blk, self.k_blk, self.v_blk,
                            self.qbar, self.kbar, self.scores, stream)
 
+    def pool_copies(self, stream=None):
+        """Block-order copies of Q, K, V with the current permutation only (no means, no
+        scores): what a step that reuses an earlier step's selection needs."""
+        P.prism_pool_score(self.q, self.k, self.v, self.perm, self.wl.block, self.q_blk, self.k_blk, self.v_blk,
+                           stream=stream)
+
     def select(self, stream=None):
-        P.prism_select(self.scores, self.sparsity, self.wl.cdf_tau, self.counts, self.idx, stream)
+        if self.fused_select:
+            P.prism_score_select(self.qbar, self.kbar, self.sparsity, self.wl.cdf_tau, self.counts, self.idx, stream)
+        else:
+            P.prism_select(self.scores, self.sparsity, self.wl.cdf_tau, self.counts, self.idx, stream)
 
     def _groups(self):
         g = self.wl.head_group or self.wl.heads

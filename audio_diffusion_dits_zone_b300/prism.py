@@ -26,12 +26,17 @@ _SIGS = {
     "prism_zone_shapes": [_P, _I32, _I64, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P, _P, _P, _SZ, _P],
     "prism_zone_shapes_noalloc": [_P, _I32, _I64, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P, _P,
                                   _P],
+    "prism_zone_partials": [_P, _I32, _I64, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _SZ, _P],
+    "prism_zone_shapes_from_partials": [_P, _I32, _I32, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _I32, _P, _P, _P,
+                                        _SZ, _P],
     "prism_pool_score": [_P, _P, _P, _I32, _I64, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _P, _P, _P, _P],
     "prism_select": [_P, _I32, _I32, ctypes.c_double, ctypes.c_double, _P, _P, _P],
+    "prism_score_select": [_P, _P, _I32, _I32, _I32, ctypes.c_double, ctypes.c_double, _P, _P, _P],
     "prism_bsa_fwd": [_P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P],
     "prism_bsa_bwd": [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _P, _SZ,
                       _P],
     "prism_a2v_norm": [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
+    "prism_attn_mse": [_P, _P, _I32, _I64, _I32, _I32, _I32, _P, _P, _SZ, _P],
     "prism_status_check": [_P, ctypes.POINTER(ctypes.c_uint32)],
     "prism_last_error": [],
     "prism_launch_count": [],
@@ -102,7 +107,8 @@ def _dtype(t):
 
 def _ld(t):
     """Token row stride (elements) of a [N, Hh, d] view with contiguous heads."""
-    assert t.dim() == 3 and t.stride(2) == 1 and t.stride(1) == t.shape[2], "need a [N, Hh, d] view, d contiguous"
+    assert t.dim() == 3 and t.stride(2) == 1 and (t.shape[1] == 1 or t.stride(1) == t.shape[2]), \
+        "need a [N, Hh, d] view, d contiguous"
     return t.stride(0)
 
 
@@ -204,6 +210,41 @@ def prism_zone_shapes_noalloc(feat, C, a2v, grid, zone, shapes, zone_shape, perm
                                            sh, len(shapes), _ptr(zone_shape), _ptr(perm), _stream(stream)))
 
 
+def prism_zone_partials(feat, C, grid, zone, partials, ws=None, stream=None):
+    """Per-zone, per-axis partial sums [Z, 3] of feat's first C channels (one rank's share
+    of the zone statistics).  feat: [N, ld].  Returns the workspace tensor it used."""
+    assert feat.dim() == 2 and feat.stride(1) == 1
+    T, H, W = grid
+    st = _stream(stream)
+
+    def call(wsp, nbytes):
+        return lib().prism_zone_partials(_ptr(feat), _dtype(feat), feat.stride(0), C, T, H, W, *zone,
+                                         _ptr(partials), wsp, nbytes, st)
+
+    ws, nbytes = _ws(call, ws, feat.device)
+    _check(call(_ptr(ws), ctypes.byref(nbytes)))
+    return ws
+
+
+def prism_zone_shapes_from_partials(partials, C_total, a2v, grid, zone, shapes, zone_shape, perm, ws=None,
+                                    stream=None):
+    """Zone shapes and permutation from gathered partial sums [n_parts, Z, 3] (summed in
+    part order) of C_total channels.  Returns the workspace tensor it used."""
+    assert partials.dim() == 3 and partials.is_contiguous() and partials.shape[2] == 3
+    T, H, W = grid
+    sh = (ctypes.c_int32 * (3 * len(shapes)))(*[int(e) for s in shapes for e in s])
+    st = _stream(stream)
+
+    def call(wsp, nbytes):
+        return lib().prism_zone_shapes_from_partials(_ptr(partials), partials.shape[0], C_total, _ptr(a2v), T, H, W,
+                                                     *zone, sh, len(shapes), _ptr(zone_shape), _ptr(perm), wsp,
+                                                     nbytes, st)
+
+    ws, nbytes = _ws(call, ws, partials.device)
+    _check(call(_ptr(ws), ctypes.byref(nbytes)))
+    return ws
+
+
 # ------------------------------------------------------------------- step 2
 def prism_pool_score(q, k, v, perm, B, q_blk=None, k_blk=None, v_blk=None, qbar=None, kbar=None, scores=None,
                      stream=None):
@@ -222,6 +263,15 @@ def prism_select(scores, sparsity, cdf_tau, counts, idx, stream=None):
     Hh, nb, _ = scores.shape
     _check(lib().prism_select(_ptr(scores), Hh, nb, float(sparsity), float(cdf_tau), _ptr(counts), _ptr(idx),
                               _stream(stream)))
+
+
+def prism_score_select(qbar, kbar, sparsity, cdf_tau, counts, idx, stream=None):
+    """Block scores and hybrid selection in one call (no score matrix).  qbar, kbar:
+    [Hh, nb, d] fp32."""
+    Hh, nb, d = qbar.shape
+    assert kbar.shape == qbar.shape and qbar.is_contiguous() and kbar.is_contiguous()
+    _check(lib().prism_score_select(_ptr(qbar), _ptr(kbar), Hh, nb, d, float(sparsity), float(cdf_tau), _ptr(counts),
+                                    _ptr(idx), _stream(stream)))
 
 
 # ------------------------------------------------------------------- step 4
@@ -272,6 +322,22 @@ def prism_bsa_bwd(q_blk, k_blk, v_blk, o_blk, do_blk, lse, B, counts, idx, dq, d
                                    _ptr(dk), _ptr(dv), wsp, nbytes, st)
 
     ws, nbytes = _ws(call, ws, q_blk.device)
+    _check(call(_ptr(ws), ctypes.byref(nbytes)))
+    return ws
+
+
+# -------------------------------------------------- attention broadcast
+def prism_attn_mse(a, b, mse, ws=None, stream=None):
+    """Per-head mean squared difference of two [N, Hh, d] tensors into mse [Hh] fp32.
+    Returns the workspace tensor it used."""
+    assert a.shape == b.shape and a.dtype == b.dtype and _ld(a) == _ld(b)
+    N, Hh, d = a.shape
+    st = _stream(stream)
+
+    def call(wsp, nbytes):
+        return lib().prism_attn_mse(_ptr(a), _ptr(b), _dtype(a), _ld(a), N, Hh, d, _ptr(mse), wsp, nbytes, st)
+
+    ws, nbytes = _ws(call, ws, a.device)
     _check(call(_ptr(ws), ctypes.byref(nbytes)))
     return ws
 

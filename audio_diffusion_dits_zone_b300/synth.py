@@ -29,6 +29,9 @@ Input recipe (the pages fix none of it; these are the readings used here):
     cycles/token + noise).  AUDIO_TOKENS = 157 audio tokens: the 81 video frames at
     16 fps span 5.06 s, taken at 31 audio latent frames per second (a reading; the
     pages give no audio token rate).
+  * Denoising trajectory (attention broadcast across diffusion steps): step t of n
+    takes x_t = (1 - sigma_t) x + sigma_t e with sigma_t = 1 - t / (n - 1) (a linear
+    rectified-flow path), x the workload's Q, K or V and e ~ N(0, 1) per (tensor, head).
   * Seeds: numpy PCG64 from SeedSequence([0, config id, tensor id, head]).
 
 Values are generated in float32; ``to_bf16`` rounds them to bfloat16 (round to
@@ -185,6 +188,33 @@ def gen_a2v_inputs(wl: Workload, heads, M: int = AUDIO_TOKENS):
     ka = np.stack([round_inputs(wl, gen_audio_head(wl, AK_ID, h, M)) for h in heads], axis=1)
     va = np.stack([round_inputs(wl, gen_audio_head(wl, AV_ID, h, M)) for h in heads], axis=1)
     return qv, ka, va
+
+
+NOISE_ID = 20  # + tensor id: the noise end of a denoising trajectory
+
+
+def trajectory_sigma(t: int, n_steps: int) -> float:
+    """Noise level of step t of an n-step denoising trajectory: 1 at the first step,
+    linearly down to 0 at the last (a rectified-flow path, as Wan's sampler takes)."""
+    return 1.0 - t / max(1, n_steps - 1)
+
+
+def gen_noise_head(wl: Workload, tensor: int, head: int) -> np.ndarray:
+    """One head of the trajectory's noise for tensor Q, K or V: float32 [N, d] ~ N(0, 1)."""
+    return _rng(wl.cid, NOISE_ID + tensor, head).standard_normal((wl.N, wl.d), dtype=np.float32)
+
+
+def gen_noise_heads(wl: Workload, tensor: int, heads, threads: int = 8) -> list:
+    """Several heads of the trajectory noise of one tensor, in parallel threads."""
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(lambda h: gen_noise_head(wl, tensor, h), list(heads)))
+
+
+def trajectory_blend(clean: np.ndarray, noise: np.ndarray, t: int, n_steps: int) -> np.ndarray:
+    """Input of step t: (1 - sigma) * clean + sigma * noise in float32, rounded like the
+    workload's inputs by the caller."""
+    sg = np.float32(trajectory_sigma(t, n_steps))
+    return (np.float32(1.0) - sg) * clean + sg * noise
 
 
 def gen_do_head(wl: Workload, head: int) -> np.ndarray:

@@ -176,7 +176,7 @@ def run_ours(args, rank, world, local_rank):
     wl = synth.WORKLOADS[args.workload]
     sp = wl.sparsity if args.sparsity is None else args.sparsity
     train = wl.mode == "fwd+bwd"
-    layer = PrismLayer(wl, dev, sparsity=sp, train=train)
+    layer = PrismLayer(wl, dev, sparsity=sp, train=train, fused_select=args.select == "fused")
     layer.load_inputs()
     layer.step()
     if P.status_check() != 0:
@@ -238,6 +238,7 @@ def run_ours(args, rank, world, local_rank):
         "zone_tma": ("hbm", wl.N * C * 2.0), "zone_partial": ("hbm", wl.N * C * 2.0),
         "pool_gather": ("hbm", 6.0 * wl.N * C * 2 + 2.0 * wl.heads * wl.nb * wl.d * 4),
         "scores": ("hbm", wl.heads * wl.nb ** 2 * 4.0 + 2.0 * wl.heads * wl.nb * wl.d * 4),
+        "score_select": ("hbm", 2.0 * wl.heads * wl.nb * wl.d * 4 + wl.heads * wl.nb * 4 + 4.0 * kept),
         "select": ("hbm", wl.heads * wl.nb ** 2 * 4.0 + wl.heads * wl.nb * 4 + 4.0 * kept),
         "bwd_prep": ("hbm", 2.0 * wl.N * C * 2 + wl.heads * wl.N * 4 + 2.0 * wl.heads * wl.nb * wl.block * 4),
     }
@@ -310,7 +311,8 @@ def run_e2e(layer, args, world):
 
     from audio_diffusion_dits_zone_b300.pipeline import PrismLayer
 
-    layers = [layer, PrismLayer(layer.wl, layer.device, sparsity=layer.sparsity, train=layer.train)]
+    layers = [layer, PrismLayer(layer.wl, layer.device, sparsity=layer.sparsity, train=layer.train,
+                                fused_select=layer.fused_select)]
 
     def ins(L):
         return [L.q, L.k, L.v, L.a2v] + ([L.do_blk] if L.train else [])
@@ -510,6 +512,116 @@ def run_a2v_reference(args):
             "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------- attention broadcast
+PAB_METRIC = "Prism attention layer with attention broadcast across diffusion steps: ms per denoising step, 720p"
+PAB_STEPS, PAB_RANGE = 30, 2
+
+
+def run_pab(args, rank, world, local_rank):
+    """A 30-step denoising trajectory of the 720p forward layer (zone shapes -> pool +
+    score -> select -> forward on every computed step) with attention broadcast: the
+    middle 70% of the steps compute attention every third step and reuse the output
+    in between.  Timed twice, with the broadcast schedule and computing every step;
+    value = ms per step with broadcast.  An untimed calibration pass measures the MSE
+    between consecutive steps' outputs (selection held) with the library's kernel."""
+    import numpy as np
+    import torch
+
+    from audio_diffusion_dits_zone_b300 import pab
+    from audio_diffusion_dits_zone_b300 import prism as P
+    from audio_diffusion_dits_zone_b300 import synth
+    from audio_diffusion_dits_zone_b300.pipeline import PrismLayer
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl, n = synth.WORKLOADS["720p"], PAB_STEPS
+    layer = PrismLayer(wl, dev, train=False)
+    layer.load_inputs()
+    # every step's Q, K, V resident before timing: (1 - sigma) x + sigma e, rounded to bf16
+    steps = [[None] * 3 for _ in range(n)]
+    for j, (tid, x) in enumerate(((synth.Q_ID, layer.q), (synth.K_ID, layer.k), (synth.V_ID, layer.v))):
+        e = torch.empty(wl.N, wl.heads, wl.d, dtype=torch.float32, device=dev)
+        for h0 in range(0, wl.heads, 8):
+            hs = list(range(h0, min(h0 + 8, wl.heads)))
+            for h, a in zip(hs, synth.gen_noise_heads(wl, tid, hs)):
+                e[:, h].copy_(torch.from_numpy(a))
+        xf = x.float()
+        for t in range(n):
+            sg = synth.trajectory_sigma(t, n)
+            steps[t][j] = ((1.0 - sg) * xf + sg * e).to(torch.bfloat16)
+        del e, xf
+    torch.cuda.synchronize()
+
+    def set_step(t):
+        layer.q, layer.k, layer.v = steps[t]
+
+    # calibration (untimed): consecutive-step MSE with the selection of step 0 held
+    with P.KernelTimer() as kt_cal:
+        curve = pab.calibrate(layer, set_step, n).double().mean(1).cpu().numpy()
+    mse_ms = statistics.mean(kt_cal.durations()["attn_mse"])
+    mse_bytes = 2.0 * wl.N * wl.heads * wl.d * 2
+
+    def trajectory(rng):
+        bl = pab.BroadcastLayer(layer, n, rng, "outputs")
+        for t in range(n):
+            set_step(t)
+            bl.run_step(t)
+        return sum(bl.plan)
+
+    for _ in range(max(1, args.warmup // 3)):
+        trajectory(PAB_RANGE)
+    torch.cuda.synchronize()
+    if P.status_check() != 0:
+        raise RuntimeError("device status word set in the warm-up")
+    res = {}
+    launches0 = P.launch_count()
+    with ClockSampler(local_rank) as clk:
+        for rng in (PAB_RANGE, 0):
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            computed = trajectory(rng)
+            t1.record()
+            torch.cuda.synchronize()
+            ms = t0.elapsed_time(t1)
+            if world > 1:
+                ms = max_over_ranks(ms, dev)
+            res[rng] = (ms / n, computed)
+    launches = P.launch_count() - launches0
+    if P.status_check() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    pk = peaks()
+    ms_pab, comp = res[PAB_RANGE]
+    ms_all = res[0][0]
+    third = max(1, len(curve) // 3)
+    line = {"metric": PAB_METRIC, "value": round(ms_pab, 3), "unit": "ms/step", "n_gpus": world, "steps": n,
+            "warmup": args.warmup, "ms_per_step": round(ms_pab, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded Wan-VAE-shaped latents blended with seeded noise along a 30-step linear path)",
+            "config": {"workload": f"pab720p: 720p Prism forward layer (T=21,H=45,W=80, {wl.N} tokens, {wl.heads} heads, "
+                                   f"d={wl.d}, bf16, sparsity {wl.sparsity}, CDF {wl.cdf_tau}) over a {n}-step "
+                                   f"denoising trajectory, attention broadcast range {PAB_RANGE} in the middle 70%",
+                       "global_batch": 1, "seq_len": wl.N, "parallelism": "replicas (one layer per GPU)",
+                       "l2": "inputs larger than L2 (every step's Q, K, V resident, 774 MB each); no flush"},
+            "computed_steps": comp, "ms_per_step_every_step": round(ms_all, 3),
+            "speedup_vs_every_step": round(ms_all / ms_pab, 3),
+            "mse_consecutive_steps": {"first_third": float(curve[:third].mean()),
+                                      "middle_third": float(curve[third:-third].mean()),
+                                      "last_third": float(curve[-third:].mean())},
+            "roofline": {"bound": "hbm", "kernel": "attn_mse", "achieved": round(mse_bytes / (mse_ms * 1e-3) / 1e9, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(mse_bytes / (mse_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4), "traffic": None,
+                         "traffic_note": "no ncu capture of this kernel",
+                         "note": "the broadcast metric's kernel; the trajectory's time is the forward layer's "
+                                 "(train720p / 720p lines)"},
+            "e2e": None, "e2e_note": "the trajectory's inputs are produced on the device step by step in a sampler; "
+                                     "no host copy belongs to a step",
+            "gpu_launches": launches, "clocks": clk.summary()}
+    return line
+
+
 # ------------------------------------------------------------ the oracle
 def oracle_sample_step(wl, sp, ctx, qblocks):
     """One bounded sample of the step on the CPU oracle: block means and scores of one
@@ -583,9 +695,44 @@ def cpu_baseline(wl, sp, budget_s=20.0, head=0):
                       f"over this head's channels done once outside the timing"}
 
 
+def run_pab_reference(args):
+    """--impl reference for the broadcast trajectory: the oracle's rate on the 720p
+    forward layer (bounded sample per step), turned into ms per denoising step for the
+    trajectory's computed steps (extrapolated from the sampled work: the sampled query
+    blocks' executed pairs scaled to all blocks and heads)."""
+    import numpy as np
+
+    from audio_diffusion_dits_zone_b300 import pab, synth
+
+    wl = synth.WORKLOADS["720p"]
+    ctx = oracle_context(wl, 0)
+    blocks = list(range(0, wl.nb, max(1, wl.nb // 64)))
+    work, dt, nblk = 0.0, 0.0, 0
+    for s in range(max(1, args.steps)):
+        b = blocks[(s * 2) % len(blocks):][:2]
+        t0 = time.perf_counter()
+        work += oracle_sample_step(wl, wl.sparsity, ctx, b)
+        dt += time.perf_counter() - t0
+        nblk += len(b)
+    rate = work / dt  # FLOP/s of the oracle
+    step_flops = work / nblk * wl.nb * wl.heads  # one computed step's forward, extrapolated
+    frac = sum(pab.schedule(PAB_STEPS, PAB_RANGE)) / PAB_STEPS
+    ms = frac * step_flops / rate * 1e3
+    return {"metric": PAB_METRIC, "value": round(ms, 1), "unit": "ms/step", "n_gpus": args.gpus, "steps": PAB_STEPS,
+            "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "pab720p (see the library's line); oracle time extrapolated from a bounded sample"},
+            "cpu_baseline": {"value": round(ms, 1), "unit": "ms/step", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": f"{nblk} query blocks of head 0 of the 720p forward layer in {dt:.1f} s, "
+                                       f"scaled to {wl.nb} blocks x {wl.heads} heads per computed step"},
+            "e2e": {"value": round(ms, 1), "unit": "ms/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def run_reference(args):
     from audio_diffusion_dits_zone_b300 import synth
 
+    if args.workload == "pab720p":
+        return run_pab_reference(args)
     wl = synth.WORKLOADS[args.workload]
     sp = wl.sparsity if args.sparsity is None else args.sparsity
     ctx = oracle_context(wl, 0)
@@ -622,6 +769,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (extra workloads)")
+    ap.add_argument("--select", default="split", choices=["fused", "split"],
+                    help="block scores + selection in one kernel (fused) or scores written, then selection (split)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -635,7 +784,8 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    line = (run_a2v if a2v else run_ours)(args, rank, world, local_rank)
+    run = run_a2v if a2v else (run_pab if args.workload == "pab720p" else run_ours)
+    line = run(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

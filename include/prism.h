@@ -93,6 +93,38 @@ int prism_zone_shapes(const void* feat, int32_t feat_dtype, int64_t feat_ld, int
                       void* ws, size_t* ws_bytes, void* stream);
 
 /*
+ * The zone step split over channels, for a layer whose heads (hence V's channels) are
+ * spread over several GPUs (the Prism page, "Data preparation and training procedure",
+ * paragraph 3, trains with FSDP and sequence parallelism; a head-sharded layer is the
+ * form in which attention itself splits): every rank calls prism_zone_partials on its own channels,
+ * the ranks gather the [Z][3] results (e.g. torch.distributed.all_gather), and every
+ * rank calls prism_zone_shapes_from_partials on the gathered [n_parts][Z][3] array.
+ * The partial sums are additive over channels (the definition of v_a above is a mean
+ * over channels of per-channel sums), so the result is prism_zone_shapes' up to the
+ * fp32 summation order; every rank that passes the same gathered array gets the same
+ * shapes and permutation, because the parts are summed in index order.
+ *
+ * prism_zone_partials -- partials[z][a] = sum over this call's C channels c and over the
+ *   zone's lines l along axis a of sum_{k in l} (F[k][c] - mean_l F[.][c])^2  (fp32).
+ *   feat, feat_dtype, feat_ld, C, grid and zone extents as in prism_zone_shapes.
+ *   partials  out [Z][3] fp32 device array.  ws: workspace (NULL = size query).
+ *
+ * prism_zone_shapes_from_partials -- zone shapes and permutation from n_parts partial
+ *   arrays [n_parts][Z][3] (device, summed in order p = 0 .. n_parts - 1) of C_total
+ *   channels in all, and the A2V field a2v [N]; v_a(z) = sum / (C_total * tokens of z).
+ *   Shapes, zone_shape and perm as in prism_zone_shapes.  1 <= n_parts <= 4096.
+ */
+int prism_zone_partials(const void* feat, int32_t feat_dtype, int64_t feat_ld, int32_t C,
+                        int32_t T, int32_t H, int32_t W, int32_t zt, int32_t zh, int32_t zw,
+                        float* partials, void* ws, size_t* ws_bytes, void* stream);
+int prism_zone_shapes_from_partials(const float* partials, int32_t n_parts, int32_t C_total,
+                                    const float* a2v, int32_t T, int32_t H, int32_t W,
+                                    int32_t zt, int32_t zh, int32_t zw,
+                                    const int32_t* shapes, int32_t n_shapes,
+                                    int32_t* zone_shape, int32_t* perm,
+                                    void* ws, size_t* ws_bytes, void* stream);
+
+/*
  * prism_zone_shapes_noalloc -- the same computation and outputs as
  * prism_zone_shapes, for callers that cannot give the library device memory (their
  * device memory belongs to another allocator, or they run in a hook that must not
@@ -149,6 +181,22 @@ int prism_pool_score(const void* q, const void* k, const void* v, int32_t dtype,
  */
 int prism_select(const float* scores, int32_t Hh, int32_t nb, double sparsity, double cdf_tau,
                  int32_t* counts, int32_t* idx, void* stream);
+
+/*
+ * prism_score_select -- steps 2 (scores) and 3 (selection) in one call, from the block
+ * means of prism_pool_score, without the [Hh][nb][nb] score matrix: each kernel block
+ * keeps its score rows on chip and selects from them.  Same readings, arithmetic and
+ * result as prism_pool_score's scores followed by prism_select (Prism page,
+ * "Region-adapted block construction", paragraph 2): scores qbar . kbar / sqrt(d)
+ * summed in fp32 over channels in ascending order, the kept set the first max(k, m)
+ * blocks of the (score desc, index asc) order; the lists equal theirs bit for bit.
+ *
+ * qbar, kbar  [Hh][nb][d] fp32, 16-byte aligned.   sparsity in [0, 1); cdf_tau in [0, 1].
+ * counts, idx as prism_select (idx row stride nb; entries past counts left untouched).
+ * Limits: d a multiple of 8, d <= 256; nb <= 4096.  No workspace.
+ */
+int prism_score_select(const float* qbar, const float* kbar, int32_t Hh, int32_t nb, int32_t d,
+                       double sparsity, double cdf_tau, int32_t* counts, int32_t* idx, void* stream);
 
 /*
  * prism_bsa_fwd -- step 4: block-sparse attention forward (Prism BSA, same page,
@@ -214,6 +262,22 @@ int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk,
                   int64_t ld, int32_t N, int32_t Hh, int32_t d, int32_t B,
                   const int32_t* counts, const int32_t* idx, int32_t nb,
                   void* dq, void* dk, void* dv, void* ws, size_t* ws_bytes, void* stream);
+
+/*
+ * prism_attn_mse -- per-head mean squared difference of two attention outputs:
+ *   mse[h] = (1 / (N d)) sum_{n, c} (a[n][h][c] - b[n][h][c])^2.
+ * The measure that decides how far attention outputs may be broadcast to later
+ * diffusion steps ("Real-time video generation with pyramid attention broadcast",
+ * method: the MSE between consecutive steps' attention outputs; their difference is
+ * small through the middle of the schedule, so outputs computed there are reused).
+ *
+ * a, b    [N][Hh][d] with row stride ld, dtype PRISM_BF16 or PRISM_F32 (both the same).
+ * mse     out [Hh] fp32 (summed in fp64 in a fixed order: the same inputs give the
+ *         same bits).
+ * ws      workspace (NULL = size query): per-head partial sums.
+ */
+int prism_attn_mse(const void* a, const void* b, int32_t dtype, int64_t ld, int32_t N, int32_t Hh,
+                   int32_t d, float* mse, void* ws, size_t* ws_bytes, void* stream);
 
 /*
  * prism_status_check -- synchronise `stream`, return PRISM_OK if the device status

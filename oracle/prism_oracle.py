@@ -415,3 +415,34 @@ def bsa_backward_sampled(Qb, Kb, Vb, dO, counts, idx, B, h, qblocks, kblocks, tl
                 dk[int(j)] += dS[:, off:off + n].T @ q * scale
             off += n
     return dq, dk, dv
+
+
+# -------------------------------------------------- attention broadcast (PAB)
+def attn_mse(A, B):
+    """mse[h] = mean over tokens n and channels c of (A[n, h, c] - B[n, h, c])^2.
+
+    The difference measure between the attention outputs of two diffusion steps that
+    the "Real-time video generation with pyramid attention broadcast" page uses to
+    choose broadcast ranges (method section: MSE between consecutive steps' attention
+    outputs).  A, B are [N, Hh, d].
+    """
+    D = np.asarray(A, np.float64) - np.asarray(B, np.float64)
+    return (D * D).mean(axis=(0, 2))
+
+
+def pab_schedule(n_steps: int, broadcast_range: int, window=(0.15, 0.85)):
+    """Per diffusion step: True where attention is computed, False where the previous
+    computed output is broadcast (reused).
+
+    Same page: the difference between consecutive steps' attention outputs is
+    U-shaped, small through the middle 70% of the steps, so outputs computed there are
+    broadcast to the following steps.  Readings: the middle window is steps
+    [round(0.15 T), round(0.85 T)); inside it attention is computed at the window's
+    first step and then every (range + 1) steps, each computed output serving the
+    `range` steps after it; every step outside the window computes.
+    """
+    lo, hi = int(round(window[0] * n_steps)), int(round(window[1] * n_steps))
+    out = []
+    for t in range(n_steps):
+        out.append(not (lo <= t < hi) or (t - lo) % (broadcast_range + 1) == 0)
+    return out

@@ -319,3 +319,20 @@ def test_bounded_wait_times_out_and_context_survives():
     P.prism_selftest_umma(ta, ta, os_, oo, 0)
     assert P.status_check() == 0
     np.testing.assert_allclose(os_.cpu().numpy(), a.astype(np.float64) @ a.astype(np.float64).T, atol=1e-3)
+
+
+def test_bsa_bwd_split_kernels_match_oracle():
+    # The library's default backward is the fused kernel (dQ reduce-added in fp32); the
+    # split kernels (dQ recomputing S and dP per query block) are selected for a whole
+    # process by PRISM_BWD_SPLIT=1.  Run that process and compare it to the oracle too.
+    import os
+    import subprocess
+    import sys
+
+    code = (
+        "import sys; sys.path.insert(0, 'tests'); import test_gpu_units as t;"
+        "t.test_bsa_bwd_tensor_core_random_lists(2048, 3, 1); t.test_bsa_bwd_dense_matches_sdpa_autograd(); print('split ok')")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PRISM_BWD_SPLIT="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "split ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]

@@ -147,6 +147,14 @@ def test_forward_workload(name):
     # property at any size: every kept list holds at least k blocks and at most nb, ascending
     c = layer.counts.cpu().numpy()
     assert c.min() >= po.keep_count_topk(wl.nb, wl.sparsity) and c.max() <= wl.nb
+    # the fused score + selection call gives the same lists for every head, bit for bit
+    counts = torch.empty_like(layer.counts)
+    idx = torch.full_like(layer.idx, -1)
+    P.prism_score_select(layer.qbar, layer.kbar, wl.sparsity, wl.cdf_tau, counts, idx)
+    assert P.status_check() == 0
+    assert torch.equal(counts, layer.counts)
+    valid = torch.arange(wl.nb, device=counts.device)[None, None, :] < counts[:, :, None]
+    assert torch.equal(torch.where(valid, idx, -1), torch.where(valid, layer.idx, -1))
 
 
 @pytest.mark.parametrize("sp", [0.80, 0.0, 0.75, 0.85, 0.93])
