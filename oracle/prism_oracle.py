@@ -169,6 +169,33 @@ def block_permutation(grid, zext, zone_shape, shapes) -> np.ndarray:
     return np.concatenate(out).astype(np.int64)
 
 
+def zone_token_counts(grid, zext) -> np.ndarray:
+    """Tokens of every zone, raster zone order (R1)."""
+    return np.array([(t1 - t0) * (h1 - h0) * (w1 - w0) for t0, t1, h0, h1, w0, w1 in zone_boxes(grid, zext)],
+                    dtype=np.int64)
+
+
+def block_permutation_chunked(grid, zext, zone_shape, shapes, B):
+    """Zone-chunked blocks, the alternative reading of R5: the same token order as
+    block_permutation, but every zone's run is cut into B-token blocks of its own (the
+    last one short), so that no block holds tokens of two zones.
+
+    Returned in a padded block order: each zone's run is followed by -1 entries up to a
+    multiple of B, so block b is positions [b B, (b + 1) B) and its blen[b] tokens are
+    the first ones.  Returns (perm_padded [Np] with -1 for padding, blen [nb])."""
+    perm = block_permutation(grid, zext, zone_shape, shapes)
+    out, blen, off = [], [], 0
+    for n in zone_token_counts(grid, zext):
+        run = perm[off:off + n]
+        off += n
+        nblk = -(-int(n) // B)
+        padded = np.full(nblk * B, -1, dtype=np.int64)
+        padded[:n] = run
+        out.append(padded)
+        blen.extend(min(B, int(n) - k * B) for k in range(nblk))
+    return np.concatenate(out), np.array(blen, dtype=np.int64)
+
+
 def zone_shapes(feature_chunks, a2v, grid, zext, shapes):
     """Step 1 of the path: (zone_shape[Z], perm[N], details) from V and the A2V field."""
     v = zone_video_variation(feature_chunks, grid, zext)
@@ -187,16 +214,18 @@ def block_lengths(N: int, B: int) -> np.ndarray:
     return lens
 
 
-def block_mean(X_blk: np.ndarray, B: int) -> np.ndarray:
+def block_mean(X_blk: np.ndarray, B: int, blen=None) -> np.ndarray:
     """Xbar[h, b, :] = mean over the tokens of block b of X_blk[:, h, :] (R6).
 
-    X_blk is [N, Hh, d] in block order.
+    X_blk is [N, Hh, d] in block order; with blen (zone-chunked blocks) block b is the
+    first blen[b] rows of positions [b B, (b + 1) B).
     """
     N, Hh, d = X_blk.shape
     nb = -(-N // B)
     out = np.empty((Hh, nb, d))
     for b in range(nb):
-        out[:, b, :] = np.asarray(X_blk[b * B:(b + 1) * B], dtype=np.float64).mean(axis=0)
+        e = (b + 1) * B if blen is None else b * B + int(blen[b])
+        out[:, b, :] = np.asarray(X_blk[b * B:e], dtype=np.float64).mean(axis=0)
     return out
 
 
@@ -264,11 +293,18 @@ def select(scores, sparsity: float, cdf_tau: float):
 
 
 # ------------------------------------------------------------------------ attention
-def kept_tokens(kept_blocks, B: int, N: int) -> np.ndarray:
+def block_rows(j, B: int, N: int, blen=None) -> np.ndarray:
+    """Token positions (block order) of block j: the B-token chunk (the last one short),
+    or the first blen[j] positions of the chunk for zone-chunked blocks."""
+    e = min((j + 1) * B, N) if blen is None else j * B + int(blen[j])
+    return np.arange(j * B, e)
+
+
+def kept_tokens(kept_blocks, B: int, N: int, blen=None) -> np.ndarray:
     """Token positions (block order) covered by a list of blocks."""
     if len(kept_blocks) == 0:
         return np.zeros(0, dtype=np.int64)
-    return np.concatenate([np.arange(j * B, min((j + 1) * B, N)) for j in kept_blocks])
+    return np.concatenate([block_rows(int(j), B, N, blen) for j in kept_blocks])
 
 
 def attention_row_block(q, Kc, Vc, scale):
@@ -282,11 +318,13 @@ def attention_row_block(q, Kc, Vc, scale):
     return (P @ Vc) / l, (m + np.log(l))[:, 0]
 
 
-def bsa_forward(Qb, Kb, Vb, counts, idx, B, heads=None, qblocks=None):
+def bsa_forward(Qb, Kb, Vb, counts, idx, B, heads=None, qblocks=None, blen=None):
     """Step 4: O[N, Hh, d] and LSE[Hh, N] over the kept blocks (R8).
 
     Inputs are in block order.  ``heads`` / ``qblocks`` restrict the work to a
-    sample; rows outside it are left as NaN.
+    sample; rows outside it are left as NaN.  With ``blen`` (zone-chunked blocks in a
+    padded block order) only the first blen[b] positions of block b are tokens; padding
+    positions are neither queries nor keys and stay NaN.
     """
     N, Hh, d = Qb.shape
     nb = -(-N // B)
@@ -295,8 +333,8 @@ def bsa_forward(Qb, Kb, Vb, counts, idx, B, heads=None, qblocks=None):
     LSE = np.full((Hh, N), np.nan)
     for h in (range(Hh) if heads is None else heads):
         for i in (range(nb) if qblocks is None else qblocks):
-            rows = np.arange(i * B, min((i + 1) * B, N))
-            cols = kept_tokens(idx[h, i, : counts[h, i]], B, N)
+            rows = block_rows(i, B, N, blen)
+            cols = kept_tokens(idx[h, i, : counts[h, i]], B, N, blen)
             o, lse = attention_row_block(np.asarray(Qb[rows, h], np.float64),
                                          np.asarray(Kb[cols, h], np.float64),
                                          np.asarray(Vb[cols, h], np.float64), scale)
@@ -324,13 +362,14 @@ def a2v_field(Qv, Ka, Va, rows=None):
     return np.sqrt((O * O).sum(axis=(1, 2))), O
 
 
-def bsa_backward(Qb, Kb, Vb, O, dO, LSE, counts, idx, B, heads=None, qblocks=None):
+def bsa_backward(Qb, Kb, Vb, O, dO, LSE, counts, idx, B, heads=None, qblocks=None, blen=None):
     """Step 5: dQ, dK, dV for the same kept lists (R8).
 
     P = exp(S - LSE), dV = P^T dO, dP = dO V^T, D = rowsum(dO * O),
     dS = P * (dP - D), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d).
     ``heads`` / ``qblocks`` restrict the work to the contributions of a sample of
-    query blocks (dK and dV then hold only those contributions).
+    query blocks (dK and dV then hold only those contributions).  ``blen`` as in
+    bsa_forward (padding positions get zero gradients).
     """
     N, Hh, d = Qb.shape
     nb = -(-N // B)
@@ -340,8 +379,8 @@ def bsa_backward(Qb, Kb, Vb, O, dO, LSE, counts, idx, B, heads=None, qblocks=Non
     dV = np.zeros((N, Hh, d))
     for h in (range(Hh) if heads is None else heads):
         for i in (range(nb) if qblocks is None else qblocks):
-            rows = np.arange(i * B, min((i + 1) * B, N))
-            cols = kept_tokens(idx[h, i, : counts[h, i]], B, N)
+            rows = block_rows(i, B, N, blen)
+            cols = kept_tokens(idx[h, i, : counts[h, i]], B, N, blen)
             if cols.size == 0:
                 continue
             q = np.asarray(Qb[rows, h], np.float64)
