@@ -44,8 +44,8 @@ __device__ void stage_tile(float* dst, const T* src, int64_t ld, int h, int D, i
 template <typename T, int D, int TPR>
 __global__ void bsa_fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                                     int64_t ld, int N, int B, const int32_t* __restrict__ counts,
-                                    const int32_t* __restrict__ idx, int nb, T* __restrict__ o,
-                                    float* __restrict__ lse, uint32_t* status) {
+                                    const int32_t* __restrict__ idx, int nb, const int32_t* __restrict__ blen,
+                                    T* __restrict__ o, float* __restrict__ lse, uint32_t* status) {
   constexpr int DP = D / TPR;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -53,7 +53,7 @@ __global__ void bsa_fwd_simt_kernel(const T* __restrict__ q, const T* __restrict
   const int i = blockIdx.x, h = blockIdx.y;
   const int r = threadIdx.x / TPR, part = threadIdx.x % TPR;
   const int row = i * B + r;
-  const bool valid = r < B && row < N;
+  const bool valid = r < B && row < N && (!blen || r < blen[i]);  // padding rows are no queries
   const float sl2 = kLog2e * rsqrtf((float)D);
   float qv[DP], acc[DP];
 #pragma unroll
@@ -71,7 +71,7 @@ __global__ void bsa_fwd_simt_kernel(const T* __restrict__ q, const T* __restrict
       if (threadIdx.x == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
       continue;
     }
-    const int len = min(B, N - j * B);
+    const int len = blen ? min(B, max(0, blen[j])) : min(B, N - j * B);
     __syncthreads();
     stage_tile<T>(Ks, k, ld, h, D, j * B, len, B);
     stage_tile<T>(Vs, v, ld, h, D, j * B, len, B);
@@ -104,7 +104,7 @@ __global__ void bsa_dq_simt_kernel(const T* __restrict__ q, const T* __restrict_
                                    const T* __restrict__ dO, const float* __restrict__ lse,
                                    const float* __restrict__ Drow, int64_t ld, int N, int B,
                                    const int32_t* __restrict__ counts, const int32_t* __restrict__ idx, int nb,
-                                   T* __restrict__ dq) {
+                                   const int32_t* __restrict__ blen, T* __restrict__ dq) {
   constexpr int DP = D / TPR;
   extern __shared__ float sm[];
   float* Ks = sm;
@@ -112,7 +112,7 @@ __global__ void bsa_dq_simt_kernel(const T* __restrict__ q, const T* __restrict_
   const int i = blockIdx.x, h = blockIdx.y;
   const int r = threadIdx.x / TPR, part = threadIdx.x % TPR;
   const int row = i * B + r;
-  const bool valid = r < B && row < N;
+  const bool valid = r < B && row < N && (!blen || r < blen[i]);  // padding rows are no queries
   const float scale = rsqrtf((float)D);
   float qv[DP], gv[DP], acc[DP];
 #pragma unroll
@@ -130,7 +130,7 @@ __global__ void bsa_dq_simt_kernel(const T* __restrict__ q, const T* __restrict_
   for (int t = 0; t < cnt; ++t) {
     const int j = lst[t];
     if (j < 0 || j >= nb) continue;
-    const int len = min(B, N - j * B);
+    const int len = blen ? min(B, max(0, blen[j])) : min(B, N - j * B);
     __syncthreads();
     stage_tile<T>(Ks, k, ld, h, D, j * B, len, B);
     stage_tile<T>(Vs, v, ld, h, D, j * B, len, B);
@@ -162,7 +162,7 @@ __global__ void bsa_dkdv_simt_kernel(const T* __restrict__ q, const T* __restric
                                      const T* __restrict__ dO, const float* __restrict__ lse,
                                      const float* __restrict__ Drow, int64_t ld, int N, int B,
                                      const int32_t* __restrict__ tcounts, const int32_t* __restrict__ tidx, int nb,
-                                     T* __restrict__ dk, T* __restrict__ dv) {
+                                     const int32_t* __restrict__ blen, T* __restrict__ dk, T* __restrict__ dv) {
   constexpr int DP = D / TPR;
   extern __shared__ float sm[];
   float* Qs = sm;
@@ -174,7 +174,7 @@ __global__ void bsa_dkdv_simt_kernel(const T* __restrict__ q, const T* __restric
   const int j = blockIdx.x / splits, sub = blockIdx.x - (blockIdx.x / splits) * splits, h = blockIdx.y;
   const int c = sub * kRowsPerCta + threadIdx.x / TPR, part = threadIdx.x % TPR;
   const int col = j * B + c;
-  const bool valid = c < B && col < N;
+  const bool valid = c < B && col < N && (!blen || c < blen[j]);  // padding rows are no keys
   const float scale = rsqrtf((float)D);
   float kv[DP], vv[DP], gk[DP], gvv[DP];
 #pragma unroll
@@ -190,7 +190,7 @@ __global__ void bsa_dkdv_simt_kernel(const T* __restrict__ q, const T* __restric
   const int32_t* lst = tidx + (size_t)hcol * nb;
   for (int t = 0; t < cnt; ++t) {
     const int i = lst[t];
-    const int len = min(B, N - i * B);
+    const int len = blen ? min(B, max(0, blen[i])) : min(B, N - i * B);
     __syncthreads();
     stage_tile<T>(Qs, q, ld, h, D, i * B, len, B);
     stage_tile<T>(Gs, dO, ld, h, D, i * B, len, B);
@@ -230,8 +230,8 @@ __global__ void bsa_dkdv_simt_kernel(const T* __restrict__ q, const T* __restric
 
 template <typename T, int D>
 cudaError_t fwd_t(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh, int B,
-                  const int32_t* counts, const int32_t* idx, int nb, void* o, float* lse, cudaStream_t st,
-                  uint32_t* status) {
+                  const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen, void* o, float* lse,
+                  cudaStream_t st, uint32_t* status) {
   constexpr int TPR = 2;
   auto kern = bsa_fwd_simt_kernel<T, D, TPR>;
   const size_t smem = (size_t)2 * B * D * sizeof(float);
@@ -239,15 +239,16 @@ cudaError_t fwd_t(const void* q, const void* k, const void* v, int64_t ld, int N
   if (e != cudaSuccess) return e;
   HookScope hs("bsa_fwd_simt", st);
   kern<<<dim3(nb, Hh), B * TPR, smem, st>>>(static_cast<const T*>(q), static_cast<const T*>(k),
-                                             static_cast<const T*>(v), ld, N, B, counts, idx, nb,
+                                             static_cast<const T*>(v), ld, N, B, counts, idx, nb, blen,
                                              static_cast<T*>(o), lse, status);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
 cudaError_t bwd_t(const void* q, const void* k, const void* v, const void* dO, const float* lse, int64_t ld, int N,
-                  int Hh, int B, const int32_t* counts, const int32_t* idx, int nb, void* dq, void* dk, void* dv,
-                  const int32_t* tcounts, const int32_t* tidx, const float* Drow, cudaStream_t st) {
+                  int Hh, int B, const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen, void* dq,
+                  void* dk, void* dv, const int32_t* tcounts, const int32_t* tidx, const float* Drow,
+                  cudaStream_t st) {
   constexpr int TPR_Q = 2, TPR_K = 4;
   auto kq = bsa_dq_simt_kernel<T, D, TPR_Q>;
   auto kk = bsa_dkdv_simt_kernel<T, D, TPR_K>;
@@ -261,45 +262,46 @@ cudaError_t bwd_t(const void* q, const void* k, const void* v, const void* dO, c
   HookScope hs("bsa_dq_simt", st);
   kq<<<dim3(nb, Hh), B * TPR_Q, smem_q, st>>>(static_cast<const T*>(q), static_cast<const T*>(k),
                                                static_cast<const T*>(v), static_cast<const T*>(dO), lse, Drow, ld,
-                                               N, B, counts, idx, nb, static_cast<T*>(dq));
+                                               N, B, counts, idx, nb, blen, static_cast<T*>(dq));
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   HookScope hs("bsa_dkdv_simt", st);
   const int splits = B > kRowsPerCta ? B / kRowsPerCta : 1;
   kk<<<dim3(nb * splits, Hh), (B / splits) * TPR_K, smem_k, st>>>(static_cast<const T*>(q), static_cast<const T*>(k),
                                                static_cast<const T*>(v), static_cast<const T*>(dO), lse, Drow, ld,
-                                               N, B, tcounts, tidx, nb, static_cast<T*>(dk), static_cast<T*>(dv));
+                                               N, B, tcounts, tidx, nb, blen, static_cast<T*>(dk),
+                                               static_cast<T*>(dv));
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t bsa_fwd_simt_launch(const void* q, const void* k, const void* v, int dtype, int64_t ld, int N, int Hh,
-                                int d, int B, const int32_t* counts, const int32_t* idx, int nb, void* o,
-                                float* lse, cudaStream_t st, uint32_t* status) {
+                                int d, int B, const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen,
+                                void* o, float* lse, cudaStream_t st, uint32_t* status) {
   if (dtype == PRISM_BF16)
-    return d == 64 ? fwd_t<__nv_bfloat16, 64>(q, k, v, ld, N, Hh, B, counts, idx, nb, o, lse, st, status)
-                   : fwd_t<__nv_bfloat16, 128>(q, k, v, ld, N, Hh, B, counts, idx, nb, o, lse, st, status);
-  return d == 64 ? fwd_t<float, 64>(q, k, v, ld, N, Hh, B, counts, idx, nb, o, lse, st, status)
-                 : fwd_t<float, 128>(q, k, v, ld, N, Hh, B, counts, idx, nb, o, lse, st, status);
+    return d == 64 ? fwd_t<__nv_bfloat16, 64>(q, k, v, ld, N, Hh, B, counts, idx, nb, blen, o, lse, st, status)
+                   : fwd_t<__nv_bfloat16, 128>(q, k, v, ld, N, Hh, B, counts, idx, nb, blen, o, lse, st, status);
+  return d == 64 ? fwd_t<float, 64>(q, k, v, ld, N, Hh, B, counts, idx, nb, blen, o, lse, st, status)
+                 : fwd_t<float, 128>(q, k, v, ld, N, Hh, B, counts, idx, nb, blen, o, lse, st, status);
 }
 
 cudaError_t bsa_bwd_simt_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                                 const float* lse, int dtype, int64_t ld, int N, int Hh, int d, int B,
-                                const int32_t* counts, const int32_t* idx, int nb, void* dq, void* dk, void* dv,
-                                const int32_t* tcounts, const int32_t* tidx, float* Drow, cudaStream_t st,
-                                uint32_t* /*status*/) {
+                                const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen, void* dq,
+                                void* dk, void* dv, const int32_t* tcounts, const int32_t* tidx, float* Drow,
+                                cudaStream_t st, uint32_t* /*status*/) {
   cudaError_t e = row_dot_launch(o, dO, dtype, ld, N, Hh, d, Drow, st);
   if (e != cudaSuccess) return e;
   if (dtype == PRISM_BF16)
-    return d == 64 ? bwd_t<__nv_bfloat16, 64>(q, k, v, dO, lse, ld, N, Hh, B, counts, idx, nb, dq, dk, dv, tcounts,
-                                              tidx, Drow, st)
-                   : bwd_t<__nv_bfloat16, 128>(q, k, v, dO, lse, ld, N, Hh, B, counts, idx, nb, dq, dk, dv,
+    return d == 64 ? bwd_t<__nv_bfloat16, 64>(q, k, v, dO, lse, ld, N, Hh, B, counts, idx, nb, blen, dq, dk, dv,
+                                              tcounts, tidx, Drow, st)
+                   : bwd_t<__nv_bfloat16, 128>(q, k, v, dO, lse, ld, N, Hh, B, counts, idx, nb, blen, dq, dk, dv,
                                                tcounts, tidx, Drow, st);
-  return d == 64 ? bwd_t<float, 64>(q, k, v, dO, lse, ld, N, Hh, B, counts, idx, nb, dq, dk, dv, tcounts, tidx, Drow,
-                                    st)
-                 : bwd_t<float, 128>(q, k, v, dO, lse, ld, N, Hh, B, counts, idx, nb, dq, dk, dv, tcounts, tidx,
-                                     Drow, st);
+  return d == 64 ? bwd_t<float, 64>(q, k, v, dO, lse, ld, N, Hh, B, counts, idx, nb, blen, dq, dk, dv, tcounts, tidx,
+                                    Drow, st)
+                 : bwd_t<float, 128>(q, k, v, dO, lse, ld, N, Hh, B, counts, idx, nb, blen, dq, dk, dv, tcounts,
+                                     tidx, Drow, st);
 }
 
 }  // namespace prism

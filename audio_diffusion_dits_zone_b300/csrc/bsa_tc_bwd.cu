@@ -45,23 +45,25 @@ constexpr float kScale = 0.08838834764831845f;                      // 1 / sqrt(
 // ------------------------------------------------------------------- prep
 // 16 threads per (head, padded row), 8 channels (one 16-byte load of O and of dO) each.
 // With dqacc != NULL it also clears the fused kernel's fp32 dQ accumulator
-// ([npad][Hh * d]): each thread zeroes the 8 accumulator channels it owns.
+// ([Hh][npad][d]): each thread zeroes the 8 accumulator channels it owns.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dO,
                                                        const float* __restrict__ lse, int64_t ld, int N, int Hh,
                                                        int npad, float* __restrict__ L2, float* __restrict__ Dp,
-                                                       float* __restrict__ dqacc) {
+                                                       float* __restrict__ dqacc, const int32_t* __restrict__ blen) {
   const int64_t gid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
   const int sub = threadIdx.x & 15;
   if (gid >= (int64_t)Hh * npad) return;  // 16-lane groups are whole: the group exits together
   // rows fastest within a head, so consecutive groups read consecutive token rows
   const int h = (int)(gid / npad), r = (int)(gid - (int64_t)h * npad);
   if (dqacc) {
-    float4* z = reinterpret_cast<float4*>(dqacc + (int64_t)r * Hh * kD + (int64_t)h * kD + sub * 8);
+    float4* z = reinterpret_cast<float4*>(dqacc + ((int64_t)h * npad + r) * kD + sub * 8);
     z[0] = z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float s = 0.f;
-  if (r < N) {
+  // padding rows of zone-chunked blocks are no queries: P = 0 there, like past the end
+  const bool row_ok = r < N && (!blen || (r & (kB - 1)) < blen[r / kB]);
+  if (row_ok) {
     const int64_t off = (int64_t)r * ld + (int64_t)h * kD + sub * 8;
     const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + off));
     const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + off));
@@ -78,8 +80,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(grp, s, off);
   if (sub == 0) {
     const size_t at = (size_t)h * npad + r;
-    Dp[at] = r < N ? s : 0.f;
-    L2[at] = r < N ? lse[(size_t)h * N + r] * kLog2e : INFINITY;
+    Dp[at] = row_ok ? s : 0.f;
+    L2[at] = row_ok ? lse[(size_t)h * N + r] * kLog2e : INFINITY;
   }
 }
 
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                      const float* __restrict__ L2, const float* __restrict__ Dp, int npad,
                      __nv_bfloat16* __restrict__ dq, int64_t ld, int N, const int32_t* __restrict__ counts,
-                     const int32_t* __restrict__ idx, int nb, uint32_t* status) {
+                     const int32_t* __restrict__ idx, int nb, const int32_t* __restrict__ blen, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                                        mbar_wait(smem_u32(&sm.dp_full), it & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
-      const int len = (j >= 0 && j < nb) ? min(kB, N - j * kB) : 0;
+      const int len = (j >= 0 && j < nb) ? (blen ? min(kB, max(0, blen[j])) : min(kB, N - j * kB)) : 0;
       uint32_t s0[32], s1[32], d0[32], d1[32];
       tmem_ld32(lane_base + b * 128 + c0, s0);
       tmem_ld32(lane_base + b * 128 + c0 + 32, s1);
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
                        const float* __restrict__ L2, const float* __restrict__ Dp, int npad,
                        __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int64_t ld, int N,
                        const int32_t* __restrict__ tcounts, const int32_t* __restrict__ tidx, int nb,
-                       uint32_t* status) {
+                       const int32_t* __restrict__ blen, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   DkdvSmem& sm = *reinterpret_cast<DkdvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -564,6 +566,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
     const int c = quarter * 32 + lane;  // key row of block j = TMEM lane
     const int q0 = half * 64;           // this thread's query columns q0 .. q0 + 63
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const bool key_ok = blen ? c < blen[j] : j * kB + c < N;
     const f2 scale2 = f2_make(kSl2, kSl2);
     bool ok = true;
     for (int it = 0; it < cnt; ++it) {
@@ -589,7 +592,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
             const f2 nl = u ? f2_make(-L.z, -L.w) : f2_make(-L.x, -L.y);
             float a0, a1;
             f2_split(f2_fma(f2_make(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), scale2, nl), a0, a1);
-            p[cc * 16 + 2 * q4 + u] = f2_make(fast_exp2(a0), fast_exp2(a1));
+            p[cc * 16 + 2 * q4 + u] = key_ok ? f2_make(fast_exp2(a0), fast_exp2(a1)) : f2_make(0.f, 0.f);
             pp[2 * q4 + u] = f2_pack_bf16(p[cc * 16 + 2 * q4 + u]);
           }
         }
@@ -673,16 +676,23 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
 
 // ------------------------------------------------------- fused dK, dV, dQ
 // One CTA per (head, key block j) walking the query blocks that kept j, like dkdv,
-// that also forms dQ: per query half x of query block i,
-//   S^T_x = K_j Q_x^T, dP^T_x = V_j dO_x^T (TMEM, N = 64), P^T_x and dS^T_x (bf16),
-//   dV += P^T_x dO_x, dK += dS^T_x Q_x (A from TMEM), and
-//   dQ_x^T = K_j^T dS_x^T (M = 128 channels, N = 64 queries, K = 128 keys; both
-//   operands MN-major in shared memory: K_j's tile as it was loaded, dS^T_x written
-//   by the softmax warps in the same 128-byte-swizzled layout),
-// and adds dQ_x into an fp32 accumulator in global memory ([npad][Hh * d]) with
-// 16-byte reductions issued straight from registers.  Five tile products per kept pair instead of the seven of the split
-// kernels (whose dq kernel recomputes S and dP).  The reduce-adds make dQ's summation
-// order, and so its last bits, depend on scheduling.
+// that also forms dQ.  Per kept query block i:
+//   S^T = K_j Q_i^T, dP^T = V_j dO_i^T                (TMEM, M = 128 keys, N = 128 queries)
+//   P^T, dS^T (bf16, per query half x of 64 queries, written by that half's warps)
+//   dV += P^T_x dO_x, dK += dS^T_x Q_x               (A from TMEM, K = 64 per half)
+//   dQ_i^T = K_j^T dS^T                               (M = 128 channels, N = 128 queries,
+//                                                      K = 128 keys; both operands
+//                                                      MN-major in shared memory: K_j's
+//                                                      tile as loaded, dS^T as written
+//                                                      by the softmax warps)
+// and adds dQ_i into an fp32 accumulator in global memory ([Hh][npad][d]: the head a
+// wave of CTAs works on is one contiguous range) with 16-byte reductions issued
+// straight from registers.  Five tile products per kept pair
+// instead of the seven of the split kernels (whose dq kernel recomputes S and dP), all
+// 128 x 128 x 128 (full-width products read 64 KB of operands per 512 tensor cycles,
+// which shared memory sustains; products split into 64-query halves would read 1.5x as
+// much per FLOP).  The reduce-adds make dQ's summation order, and so its last bits,
+// depend on scheduling.
 //
 // Warps: 0 TMA producer, 1 issuer of S^T and dP^T (TMEM owner), 2 issuer of dV, dK
 // and dQ^T, 3 idle; 4-7 softmax gradient of query rows 0-63 (half a) of every query
@@ -694,18 +704,18 @@ struct FusedSmem {
   uint8_t k[kTile];
   uint8_t v[kTile];
   QdoStage st[2];
-  // [query half]: dS^T_x (128 key rows x 64 queries bf16, 128-byte swizzle), the B
-  // operand of dQ_x^T
+  // dS^T (128 key rows x 128 queries bf16): [query half][128 rows x 128 bytes], each
+  // half in the 128-byte-swizzled layout of a loaded tile; the B operand of dQ^T
   uint8_t ds[2][kHalf];
   float l2[2][kB];  // lse * log2(e) of the stage's query rows
   float dr[2][kB];  // D of the stage's query rows
   uint64_t kv_full;
   uint64_t qdo_full[2], qdo_empty[2];
-  uint64_t s_full[2], dp_full[2];  // [query half]: S^T, dP^T computed
+  uint64_t s_full, dp_full;        // S^T, dP^T computed
   uint64_t p_full[2], ds_full[2];  // [query half]: P^T, dS^T written
-  uint64_t v_done[2], k_done[2];   // [query half]: dV has read P^T / dK has read dS^T
-  uint64_t dq_full[2];             // [query half]: dQ^T computed (dS^T tile read)
-  uint64_t dq_free[2];             // [query half]: dQ^T loaded by the drain (TMEM free)
+  uint64_t pair_done;              // dV and dK of the pair have read P^T and dS^T
+  uint64_t dq_full;                // dQ^T computed (the dS^T tile read)
+  uint64_t dq_free;                // dQ^T loaded by the drain (TMEM columns free)
   uint64_t acc_done, in_done;
   uint32_t tmem_base;
   int abort;
@@ -714,20 +724,20 @@ constexpr size_t kFusedSmemBytes = sizeof(FusedSmem);
 static_assert(kFusedSmemBytes <= 232448, "shared memory budget");
 static_assert(offsetof(FusedSmem, ds) % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 
-// TMEM: S^T_a [0,64) S^T_b [64,128) dP^T_a [128,192) dP^T_b [192,256) dV [256,384)
-// dK [384,512).  In the S^T_x columns the softmax writes P^T_x (bf16) over the first
-// 32 and dS^T_x over the last 32; dQ_x^T is computed into the dP^T_x columns once the
-// softmax has loaded them.  Issuer 1: S^T_a, S^T_b (each once dV and dK of the previous
-// pair have read that half's P^T, dS^T), then dP^T_a, dP^T_b (each once the drain has
-// loaded the previous dQ^T of that half).  Issuer 2 per half: dV once P^T is written;
-// dK and dQ^T once dS^T is written.
+// TMEM: S^T [0,128) (query q in column q), dP^T [128,256), dV [256,384), dK [384,512).
+// Query half x (columns 64x .. 64x + 63 of S^T) writes P^T_x (bf16) over the first 32 of
+// its own columns and dS^T_x over the last 32; dQ^T is computed into the dP^T columns
+// once both halves have loaded them.  Issuer 1: S^T once dV and dK of the previous pair
+// have completed; dP^T once the drain has loaded the previous dQ^T.  Issuer 2: dV_a,
+// dV_b as the halves' P^T are written, dK_a, dK_b as their dS^T are, then dQ^T.
 __global__ void __launch_bounds__(kFusedThreads, 1)
     bsa_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                          float* __restrict__ dqacc, const float* __restrict__ L2,
                          const float* __restrict__ Dp, int npad, __nv_bfloat16* __restrict__ dk,
                          __nv_bfloat16* __restrict__ dv, int64_t ld, int N, const int32_t* __restrict__ tcounts,
-                         const int32_t* __restrict__ tidx, int nb, uint32_t* status) {
+                         const int32_t* __restrict__ tidx, int nb, const int32_t* __restrict__ blen,
+                         uint32_t* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the swizzled tiles need it; never seen, but checked
     if (threadIdx.x == 0) flag_error(status, PRISM_DEV_TMEM);
@@ -745,15 +755,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sm.qdo_full[s]), 1);
       mbar_init(smem_u32(&sm.qdo_empty[s]), 1);
-      mbar_init(smem_u32(&sm.s_full[s]), 1);
-      mbar_init(smem_u32(&sm.dp_full[s]), 1);
       mbar_init(smem_u32(&sm.p_full[s]), 4);
       mbar_init(smem_u32(&sm.ds_full[s]), 4);
-      mbar_init(smem_u32(&sm.v_done[s]), 1);
-      mbar_init(smem_u32(&sm.k_done[s]), 1);
-      mbar_init(smem_u32(&sm.dq_full[s]), 1);
-      mbar_init(smem_u32(&sm.dq_free[s]), 4);
     }
+    mbar_init(smem_u32(&sm.s_full), 1);
+    mbar_init(smem_u32(&sm.dp_full), 1);
+    mbar_init(smem_u32(&sm.pair_done), 1);
+    mbar_init(smem_u32(&sm.dq_full), 1);
+    mbar_init(smem_u32(&sm.dq_free), 4);
     mbar_init(smem_u32(&sm.acc_done), 1);
     mbar_init(smem_u32(&sm.in_done), 1);
     sm.abort = 0;
@@ -804,7 +813,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ issuer of S^T and dP^T
     if (lane == 0 && cnt > 0) {
-      constexpr uint32_t id_h = idesc_bf16_f32(kB, 64, false, false);  // M = 128 keys, N = 64 queries
+      constexpr uint32_t id_ss = idesc_bf16_f32(kB, kB, false, false);  // M = 128 keys, N = 128 queries
       const uint64_t dk_k = smem_desc(smem_u32(sm.k), 16, 1024, kSwizzle128B);
       const uint64_t dk_v = smem_desc(smem_u32(sm.v), 16, 1024, kSwizzle128B);
       const uint64_t dq0 = smem_desc(smem_u32(sm.st[0].q), 16, 1024, kSwizzle128B);
@@ -813,34 +822,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, abort, status);
       for (int it = 0; ok && it < cnt; ++it) {
         const int s = it & 1;
-        if (!(ok = mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status))) break;
         const uint32_t so = s * (uint32_t)sizeof(QdoStage);
+        if (!(ok = mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status))) break;
+        // S^T overwrites the P^T / dS^T that the previous pair's dV / dK read
+        if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.pair_done), (it - 1) & 1, abort, status))) break;
+        tc_fence_after();
+        const uint64_t dq = desc_at(dq0, so), ddo = desc_at(ddo0, so);
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          // S^T_x overwrites the P^T_x / dS^T_x that the previous pair's dV / dK read
-          if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.v_done[x]), (it - 1) & 1, abort, status) &&
-                               mbar_wait(smem_u32(&sm.k_done[x]), (it - 1) & 1, abort, status)))
-            break;
-          tc_fence_after();
-          // the half's rows of the Q / dO tiles start 64 rows (8 KB) into each box
-          const uint64_t dq = desc_at(dq0, so + x * 8192);
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, desc_at(dk_k, koff(kk)), desc_at(dq, koff(kk)), id_ss, kk > 0);
+        tc_commit(smem_u32(&sm.s_full));
+        // dP^T overwrites the dQ^T of the previous pair once the drain has loaded it
+        if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.dq_free), (it - 1) & 1, abort, status))) break;
+        tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + x * 64, desc_at(dk_k, koff(kk)), desc_at(dq, koff(kk)), id_h, kk > 0);
-          tc_commit(smem_u32(&sm.s_full[x]));
-        }
-        if (!ok) break;
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          // dP^T_x overwrites the dQ^T_x of the previous pair once the drain has loaded it
-          if (it > 0 && !(ok = mbar_wait(smem_u32(&sm.dq_free[x]), (it - 1) & 1, abort, status))) break;
-          tc_fence_after();
-          const uint64_t ddo = desc_at(ddo0, so + x * 8192);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + 128 + x * 64, desc_at(dk_v, koff(kk)), desc_at(ddo, koff(kk)), id_h, kk > 0);
-          tc_commit(smem_u32(&sm.dp_full[x]));
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 128, desc_at(dk_v, koff(kk)), desc_at(ddo, koff(kk)), id_ss, kk > 0);
+        tc_commit(smem_u32(&sm.dp_full));
       }
       tc_commit(smem_u32(&sm.in_done));
       drain_wait(smem_u32(&sm.in_done), 0);
@@ -849,13 +846,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // -------------------------------------------- issuer of dV, dK and dQ^T
     if (lane == 0 && cnt > 0) {
       constexpr uint32_t id_ts = idesc_bf16_f32(kB, kD, false, true);
-      constexpr uint32_t id_dq = idesc_bf16_f32(kD, 64, true, true);  // M = 128 channels, N = 64 queries
+      constexpr uint32_t id_dq = idesc_bf16_f32(kD, kB, true, true);  // M = 128 channels, N = 128 queries
       const uint64_t dqmn0 = smem_desc(smem_u32(sm.st[0].q), kHalf, 1024, kSwizzle128B);
       const uint64_t ddomn0 = smem_desc(smem_u32(sm.st[0].dO), kHalf, 1024, kSwizzle128B);
       // K_j read as K_j^T: M = channels (two 64-wide atoms kHalf apart), K = keys
       const uint64_t dkt = smem_desc(smem_u32(sm.k), kHalf, 1024, kSwizzle128B);
-      // dS^T_x: N = 64 queries (one atom), K = keys
-      const uint64_t dds0 = smem_desc(smem_u32(sm.ds[0]), kHalf, 1024, kSwizzle128B);
+      // dS^T: N = queries (two 64-wide atoms, the halves' tiles kHalf apart), K = keys
+      const uint64_t dds = smem_desc(smem_u32(sm.ds[0]), kHalf, 1024, kSwizzle128B);
       bool ok = true;
       for (int it = 0; ok && it < cnt; ++it) {
         const int s = it & 1;
@@ -869,22 +866,24 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           for (int kk = 0; kk < 4; ++kk)  // dV += P^T_x dO_x
             mma_ts(tmem + 256, tmem + x * 64 + kk * 8, desc_at(ddomn, (x * 4 + kk) * 2048), id_ts,
                    (it > 0 || x > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(smem_u32(&sm.v_done[x]));
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
           if (!(ok = mbar_wait(smem_u32(&sm.ds_full[x]), it & 1, abort, status))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // dK += dS^T_x Q_x
             mma_ts(tmem + 384, tmem + x * 64 + 32 + kk * 8, desc_at(dqmn, (x * 4 + kk) * 2048), id_ts,
                    (it > 0 || x > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(smem_u32(&sm.k_done[x]));
-          const uint64_t dds = desc_at(dds0, x * kHalf);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ_x^T = K_j^T dS_x^T
-            mma_ss(tmem + 128 + x * 64, desc_at(dkt, kk * 2048), desc_at(dds, kk * 2048), id_dq, kk > 0);
-          tc_commit(smem_u32(&sm.dq_full[x]));
         }
         if (!ok) break;
-        tc_commit(smem_u32(&sm.qdo_empty[s]));
+        tc_commit(smem_u32(&sm.pair_done));
+        tc_commit(smem_u32(&sm.qdo_empty[s]));  // dK_b was the last reader of Q_i, dO_i
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dQ^T = K_j^T dS^T
+          mma_ss(tmem + 128, desc_at(dkt, kk * 2048), desc_at(dds, kk * 2048), id_dq, kk > 0);
+        tc_commit(smem_u32(&sm.dq_full));
       }
       // every product has completed once this barrier flips
       tc_commit(smem_u32(&sm.acc_done));
@@ -897,7 +896,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int c = quarter * 32 + lane;  // key row of block j = TMEM lane
     const int q0 = x * 64;              // this thread's query columns q0 .. q0 + 63
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const bool key_ok = j * kB + c < N;  // rows past the last token (zero-filled) give nothing
+    // rows past the last token (zero-filled) or padding of zone-chunked blocks give nothing
+    const bool key_ok = blen ? c < blen[j] : j * kB + c < N;
     const uint32_t dsrow = smem_u32(sm.ds[x]) + c * 128;
     const uint32_t sw = c & 7;
     const f2 scale2 = f2_make(kSl2, kSl2);
@@ -905,7 +905,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     for (int it = 0; it < cnt; ++it) {
       const int s = it & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_full[s]), (it >> 1) & 1, abort, status) &&
-                                       mbar_wait(smem_u32(&sm.s_full[x]), it & 1, abort, status));
+                                       mbar_wait(smem_u32(&sm.s_full), it & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
       const float4* l2v = reinterpret_cast<const float4*>(sm.l2[s] + q0);
@@ -914,7 +914,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {  // 16 query columns at a time
         uint32_t sr[16];
-        tmem_ld16(lane_base + x * 64 + cc * 16, sr);
+        tmem_ld16(lane_base + q0 + cc * 16, sr);
         tmem_wait_ld();
         reg_fence16(sr);
         uint32_t pp[8];
@@ -932,22 +932,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             pp[2 * q4 + u] = f2_pack_bf16(pv);
           }
         }
-        // P^T_x over columns 8cc .. 8cc + 7 of S^T_x (already loaded above)
-        tmem_st8(lane_base + x * 64 + cc * 8, pp);
+        // P^T_x over columns q0 + 8cc .. of S^T (this half's columns, already loaded)
+        tmem_st8(lane_base + q0 + cc * 8, pp);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.p_full[x]));
       // dS^T_x overwrites the shared tile that the previous pair's dQ^T read
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dp_full[x]), it & 1, abort, status) &&
-                                       (it == 0 || mbar_wait(smem_u32(&sm.dq_full[x]), (it - 1) & 1, abort, status)));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dp_full), it & 1, abort, status) &&
+                                       (it == 0 || mbar_wait(smem_u32(&sm.dq_full), (it - 1) & 1, abort, status)));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t pr[16];
-        tmem_ld16(lane_base + 128 + x * 64 + cc * 16, pr);
+        tmem_ld16(lane_base + 128 + q0 + cc * 16, pr);
         tmem_wait_ld();
         reg_fence16(pr);
         uint32_t dd[8];
@@ -962,9 +962,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 f2_mul(p[cc * 8 + 2 * q4 + u], f2_add(f2_make(__uint_as_float(pr[e]), __uint_as_float(pr[e + 1])), nd)));
           }
         }
-        // dS^T_x over columns 32 + 8cc .. of S^T_x (A of dK) and into row c of the
-        // shared dS^T_x tile (B of dQ^T): 16-byte chunk k of the row at k ^ (c & 7)
-        tmem_st8(lane_base + x * 64 + 32 + cc * 8, dd);
+        // dS^T_x over columns q0 + 32 + 8cc .. of S^T (A of dK) and into row c of the
+        // half's shared dS^T tile (B of dQ^T): 16-byte chunk k of the row at k ^ (c & 7)
+        tmem_st8(lane_base + q0 + 32 + cc * 8, dd);
         st_shared_v4(dsrow + ((((uint32_t)(2 * cc)) ^ sw) << 4), dd[0], dd[1], dd[2], dd[3]);
         st_shared_v4(dsrow + ((((uint32_t)(2 * cc + 1)) ^ sw) << 4), dd[4], dd[5], dd[6], dd[7]);
       }
@@ -1010,34 +1010,36 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
   } else if (warp >= 12) {
     // -------------------------------------------------------------- dQ drain
-    // Thread = channel dch (TMEM lane of dQ^T).  Per query half: load the 64 query
-    // columns, free the TMEM columns, then per 4 queries transpose 4 x 4 values inside
-    // each quad of lanes (after it, lane 4g + k holds query 4s + k of channels 4g ..
-    // 4g + 3) and add them to the accumulator with 16-byte reductions: one warp
-    // instruction covers 4 query rows x 128 contiguous bytes.
+    // Thread = channel dch (TMEM lane of dQ^T).  Per pair: load the 128 query columns
+    // in two 64-column rounds (the columns are freed once both are loaded), and per 4
+    // queries transpose 4 x 4 values inside each quad of lanes (after it, lane 4g + k
+    // holds query 4s + k of channels 4g .. 4g + 3) and add them to the accumulator
+    // with 16-byte reductions: one warp instruction covers 4 query rows x 128 bytes.
     const int quarter = warp & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const int k = lane & 3, g = lane >> 2;
-    const int64_t acc_ld = (int64_t)gridDim.x / nb * kD;  // Hh * d
+    float* acc_h = dqacc + (int64_t)h * nb * kB * kD;  // this head's [npad][d]
     bool ok = true;
     for (int it = 0; ok && it < cnt; ++it) {
       int i = lst[it];
       if (i < 0 || i >= nb) i = 0;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full), it & 1, abort, status));
+      if (!ok) break;
+      tc_fence_after();
 #pragma unroll 1
-      for (int x = 0; x < 2; ++x) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full[x]), it & 1, abort, status));
-        if (!ok) break;
-        tc_fence_after();
+      for (int half = 0; half < 2; ++half) {
         uint32_t r[64];
-        tmem_ld32(lane_base + 128 + x * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld32(lane_base + 128 + x * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_ld32(lane_base + 128 + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(lane_base + 128 + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         tmem_wait_ld();
         reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
         reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free[x]));
-        float* base = dqacc + (int64_t)(i * kB + x * 64 + k) * acc_ld + (int64_t)h * kD + quarter * 32 + 4 * g;
+        if (half == 1) {  // all 128 columns read: dP^T of the next pair may overwrite them
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.dq_free));
+        }
+        float* base = acc_h + (int64_t)(i * kB + half * 64 + k) * kD + quarter * 32 + 4 * g;
 #pragma unroll
         for (int s4 = 0; s4 < 16; ++s4) {
           float v0 = __uint_as_float(r[4 * s4]), v1 = __uint_as_float(r[4 * s4 + 1]);
@@ -1057,7 +1059,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             if (odd) v0 = a, v2 = b;
             else v1 = a, v3 = b;
           }
-          red_add_v4(base + (int64_t)(4 * s4) * acc_ld, v0, v1, v2, v3);
+          red_add_v4(base + (int64_t)(4 * s4) * kD, v0, v1, v2, v3);
         }
       }
     }
@@ -1070,22 +1072,24 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
 }
 
-// dq[r][h][c] = bf16(acc[r][h * d + c] / sqrt(d)): one thread per 8 channels of a token row.
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, int Hh, int N,
+// dq[r][h][c] = bf16(acc[h][r][c] / sqrt(d)): one thread per 8 channels of a (head, token)
+// row, threads in accumulator order (contiguous reads; each row of 256 bytes written whole).
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, int Hh, int N, int npad,
                                                          __nv_bfloat16* __restrict__ dq, int64_t ld) {
-  const int64_t per_row = (int64_t)Hh * (kD / 8);
   const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (v >= (int64_t)N * per_row) return;
-  const int64_t r = v / per_row;
-  const int cv = (int)(v - r * per_row);
-  const float4* src = reinterpret_cast<const float4*>(acc + r * Hh * kD + (int64_t)cv * 8);
+  if (v >= (int64_t)Hh * N * (kD / 8)) return;
+  const int cv = (int)(v & (kD / 8 - 1));
+  const int64_t hr = v / (kD / 8);
+  const int h = (int)(hr / N);
+  const int64_t r = hr - (int64_t)h * N;
+  const float4* src = reinterpret_cast<const float4*>(acc + ((int64_t)h * npad + r) * kD + (int64_t)cv * 8);
   const float4 a = __ldcs(src), b = __ldcs(src + 1);
   uint4 o;
   o.x = pack_bf16x2(a.x * kScale, a.y * kScale);
   o.y = pack_bf16x2(a.z * kScale, a.w * kScale);
   o.z = pack_bf16x2(b.x * kScale, b.y * kScale);
   o.w = pack_bf16x2(b.z * kScale, b.w * kScale);
-  *reinterpret_cast<uint4*>(dq + r * ld + (int64_t)cv * 8) = o;
+  *reinterpret_cast<uint4*>(dq + r * ld + (int64_t)h * kD + (int64_t)cv * 8) = o;
 }
 
 }  // namespace
@@ -1096,8 +1100,8 @@ size_t bwd_tc_dqacc_bytes(int Hh, int nb) { return (size_t)nb * kB * Hh * kD * s
 cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,
                               const int32_t* idx, int nb, void* dq, void* dk, void* dv, const int32_t* tcounts,
-                              const int32_t* tidx, float* rowstats, float* dqacc, cudaStream_t st,
-                              uint32_t* status) {
+                              const int32_t* tidx, const int32_t* blen, float* rowstats, float* dqacc,
+                              cudaStream_t st, uint32_t* status) {
   const int npad = nb * kB;
   float* L2 = rowstats;
   float* Dp = rowstats + (size_t)Hh * npad;
@@ -1106,7 +1110,7 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
     HookScope hs("bwd_prep", st);
     bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, ld, N, Hh, npad, L2, Dp,
-        dqacc);
+        dqacc, blen);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -1126,13 +1130,13 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
       HookScope hs("bsa_bwd_tc", st);
       bsa_bwd_fused_kernel<<<(unsigned)Hh * nb, kFusedThreads, kFusedSmemBytes, st>>>(
           mq, mk, mv, mdo, dqacc, L2, Dp, npad, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), ld,
-          N, tcounts, tidx, nb, status);
+          N, tcounts, tidx, nb, blen, status);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t vecs = (int64_t)N * Hh * (kD / 8);
     HookScope hs("dq_convert", st);
-    dq_convert_kernel<<<(unsigned)((vecs + 255) / 256), 256, 0, st>>>(dqacc, Hh, N, static_cast<__nv_bfloat16*>(dq),
-                                                                      ld);
+    dq_convert_kernel<<<(unsigned)((vecs + 255) / 256), 256, 0, st>>>(dqacc, Hh, N, npad,
+                                                                      static_cast<__nv_bfloat16*>(dq), ld);
     return cudaGetLastError();
   }
   // split: dQ recomputes S and dP per query block; dK / dV per key block
@@ -1145,13 +1149,13 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
   {
     HookScope hs("bsa_dq_tc", st);
     bsa_dq_tc_kernel<<<(unsigned)Hh * nb, kDqThreads, kDqSmemBytes, st>>>(
-        mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dq), ld, N, counts, idx, nb, status);
+        mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dq), ld, N, counts, idx, nb, blen, status);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   HookScope hs("bsa_dkdv_tc", st);
   bsa_dkdv_tc_kernel<<<(unsigned)Hh * nb, kDkdvThreads, kDkdvSmemBytes, st>>>(
       mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), ld, N,
-      tcounts, tidx, nb, status);
+      tcounts, tidx, nb, blen, status);
   return cudaGetLastError();
 }
 

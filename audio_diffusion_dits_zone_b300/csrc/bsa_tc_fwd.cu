@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
                       float* __restrict__ lse, float* __restrict__ sqn, int64_t ld, int N, int Nk,
                       const int32_t* __restrict__ counts, const int32_t* __restrict__ idx, int nbq,
-                      int nbk, uint32_t* status) {
+                      int nbk, const int32_t* __restrict__ blen, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -321,7 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool jok = j_raw >= 0 && j_raw < nbk;
       const int j = jok ? j_raw : 0;
-      const int len = jok ? min(kBN, Nk - j * kBN) : 0;
+      // keys of block j: the first blen[j] rows (zone-chunked blocks), else the B-token
+      // chunk, the last one short
+      const int len = jok ? (blen ? min(kBN, max(0, blen[j])) : min(kBN, Nk - j * kBN)) : 0;
       if (!jok && r == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
       // the whole S row: four loads in flight, one wait
       float s[128];
@@ -585,15 +587,16 @@ cudaError_t wait_timeout_selftest_launch(uint64_t limit_ns, int* marker, cudaStr
 }
 
 cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
-                              const int32_t* counts, const int32_t* idx, int nb, void* o, float* lse,
-                              cudaStream_t st, uint32_t* status) {
-  return attn_fwd_tc_launch(q, k, v, ld, ld, N, N, Hh, counts, idx, nb, nb, o, lse, nullptr, "bsa_fwd_tc", st,
+                              const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen, void* o,
+                              float* lse, cudaStream_t st, uint32_t* status) {
+  return attn_fwd_tc_launch(q, k, v, ld, ld, N, N, Hh, counts, idx, nb, nb, blen, o, lse, nullptr, "bsa_fwd_tc", st,
                             status);
 }
 
 cudaError_t attn_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int64_t ld_kv, int N,
-                               int Nk, int Hh, const int32_t* counts, const int32_t* idx, int nbq, int nbk, void* o,
-                               float* lse, float* sqn, const char* name, cudaStream_t st, uint32_t* status) {
+                               int Nk, int Hh, const int32_t* counts, const int32_t* idx, int nbq, int nbk,
+                               const int32_t* blen, void* o, float* lse, float* sqn, const char* name,
+                               cudaStream_t st, uint32_t* status) {
   CUtensorMap mq, mk, mv;
   const uint64_t inner = (uint64_t)Hh * kD;
   if (!tensor_map_2d_bf16(&mq, q, inner, N, (uint64_t)ld * 2, 64, kBM) ||
@@ -605,7 +608,7 @@ cudaError_t attn_fwd_tc_launch(const void* q, const void* k, const void* v, int6
   if (e != cudaSuccess) return e;
   HookScope hs(name, st);
   bsa_fwd_tc_kernel<<<(unsigned)Hh * nbq, kThreads, kFwdSmemBytes, st>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, sqn, ld, N, Nk, counts, idx, nbq, nbk, status);
+      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, sqn, ld, N, Nk, counts, idx, nbq, nbk, blen, status);
   return cudaGetLastError();
 }
 

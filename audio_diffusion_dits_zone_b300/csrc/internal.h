@@ -50,10 +50,19 @@ cudaError_t zone_from_partials_launch(const float* parts, int nparts, int C_tota
                                       const ZoneGeom& g, const ShapeSet& shapes, int32_t* zone_shape, int32_t* perm,
                                       void* ws, cudaStream_t st);
 
+// Zone-chunked blocks (each zone cut into B-token blocks of its own): block count nb
+// and padded length np = nb * B; the padded permutation (-1 at padding) and the block
+// lengths from the zone shapes; ws holds Z int32.
+void zone_chunked_size(const ZoneGeom& g, int B, int64_t* nb, int64_t* np);
+cudaError_t zone_perm_chunked_launch(const int32_t* zone_shape, const ZoneGeom& g, const ShapeSet& shapes, int B,
+                                     int32_t* perm, int32_t* blen, int64_t np, void* ws, cudaStream_t st);
+
 // pool_score.cu
+// Block order of N positions from n_src source rows; perm entries -1 are padding (zero
+// rows in the copies, not counted in the block means).
 cudaError_t pool_launch(const void* q, const void* k, const void* v, int dtype, int64_t ld, const int32_t* perm,
-                        int N, int Hh, int d, int B, void* qb, void* kb, void* vb, int64_t ldb, float* qbar,
-                        float* kbar, cudaStream_t st, uint32_t* status);
+                        int n_src, int N, int Hh, int d, int B, void* qb, void* kb, void* vb, int64_t ldb,
+                        float* qbar, float* kbar, cudaStream_t st, uint32_t* status);
 cudaError_t scores_launch(const float* qbar, const float* kbar, int Hh, int nb, int d, float* scores,
                           cudaStream_t st);
 
@@ -68,13 +77,13 @@ cudaError_t score_select_launch(const float* qbar, const float* kbar, int Hh, in
 
 // bsa_simt.cu (CUDA-core attention for f32 inputs and shapes outside the tensor-core path)
 cudaError_t bsa_fwd_simt_launch(const void* q, const void* k, const void* v, int dtype, int64_t ld, int N, int Hh,
-                                int d, int B, const int32_t* counts, const int32_t* idx, int nb, void* o,
-                                float* lse, cudaStream_t st, uint32_t* status);
+                                int d, int B, const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen,
+                                void* o, float* lse, cudaStream_t st, uint32_t* status);
 cudaError_t bsa_bwd_simt_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                                 const float* lse, int dtype, int64_t ld, int N, int Hh, int d, int B,
-                                const int32_t* counts, const int32_t* idx, int nb, void* dq, void* dk, void* dv,
-                                const int32_t* tcounts, const int32_t* tidx, float* Drow, cudaStream_t st,
-                                uint32_t* status);
+                                const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen, void* dq,
+                                void* dk, void* dv, const int32_t* tcounts, const int32_t* tidx, float* Drow,
+                                cudaStream_t st, uint32_t* status);
 
 // bsa_lists.cu (transposed kept lists and the backward row statistic)
 size_t lists_ws_bytes(int Hh, int nb);
@@ -84,22 +93,25 @@ cudaError_t row_dot_launch(const void* o, const void* dO, int dtype, int64_t ld,
                            cudaStream_t st);
 
 // bsa_tc_fwd.cu / bsa_tc_bwd.cu (tcgen05 tensor-core path: bf16, d = 128, B = 128)
+// blen (nullable): tokens of each block (zone-chunked blocks); NULL = B-token chunks, the
+// last one short.
 cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
-                              const int32_t* counts, const int32_t* idx, int nb, void* o, float* lse,
-                              cudaStream_t st, uint32_t* status);
+                              const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen, void* o,
+                              float* lse, cudaStream_t st, uint32_t* status);
 // The same kernel with a key sequence of its own (Nk tokens in nbk blocks, row stride
 // ld_kv) and optional outputs: o, lse and sqn ([Hh][N] fp32, the squared L2 norm of each
 // normalised output row) may each be NULL.  counts == NULL visits every key block.
 cudaError_t attn_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int64_t ld_kv, int N,
-                               int Nk, int Hh, const int32_t* counts, const int32_t* idx, int nbq, int nbk, void* o,
-                               float* lse, float* sqn, const char* name, cudaStream_t st, uint32_t* status);
+                               int Nk, int Hh, const int32_t* counts, const int32_t* idx, int nbq, int nbk,
+                               const int32_t* blen, void* o, float* lse, float* sqn, const char* name,
+                               cudaStream_t st, uint32_t* status);
 // The cross-attention of the A2V field (a2v.cu): sqn[h][n] = |O[n][h]|^2, O optional.
 cudaError_t a2v_attn_launch(const void* qv, const void* ka, const void* va, int64_t ld_v, int64_t ld_a, int N,
                             int M, int Hh, void* o, float* sqn, cudaStream_t st, uint32_t* status);
 // a2v[n] = sqrt(sum_h sqn[h][n]).
 cudaError_t a2v_reduce_launch(const float* sqn, int N, int Hh, float* a2v, cudaStream_t st);
 size_t bwd_tc_rowstats_bytes(int Hh, int nb);
-// fp32 dQ accumulator of the fused backward: [nb * 128][Hh * 128]
+// fp32 dQ accumulator of the fused backward: [Hh][nb * 128][128]
 size_t bwd_tc_dqacc_bytes(int Hh, int nb);
 // dqacc != NULL: the fused kernel (dK, dV and dQ in one pass over the transposed lists,
 // dQ reduce-added into dqacc, then converted); dqacc == NULL: the split kernels (dQ per
@@ -107,8 +119,8 @@ size_t bwd_tc_dqacc_bytes(int Hh, int nb);
 cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,
                               const int32_t* idx, int nb, void* dq, void* dk, void* dv, const int32_t* tcounts,
-                              const int32_t* tidx, float* rowstats, float* dqacc, cudaStream_t st,
-                              uint32_t* status);
+                              const int32_t* tidx, const int32_t* blen, float* rowstats, float* dqacc,
+                              cudaStream_t st, uint32_t* status);
 
 // pab.cu: per-head mean squared difference of two [N][Hh][d] tensors (row stride ld);
 // part holds Hh * attn_mse_chunks(N, Hh) fp32 partial sums.

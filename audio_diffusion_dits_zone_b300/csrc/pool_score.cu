@@ -57,25 +57,32 @@ struct Vec<T, 1> {
 template <typename T, int VW>
 __global__ void __launch_bounds__(kPoolThreads)
     pool_gather_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int64_t ld,
-                       const int32_t* __restrict__ perm, int N, int Hh, int d, int B, T* __restrict__ qb,
+                       const int32_t* __restrict__ perm, int n_src, int N, int Hh, int d, int B, T* __restrict__ qb,
                        T* __restrict__ kb, T* __restrict__ vb, int64_t ldb, float* __restrict__ qbar,
                        float* __restrict__ kbar, int nb, uint32_t* status) {
   using R = typename Vec<T, VW>::raw;
-  extern __shared__ int32_t rows[];  // source row of each block-order row
+  extern __shared__ int32_t rows[];  // source row of each block-order row (-1: padding)
+  __shared__ int nvalid;
   const int b = blockIdx.x;
   const int r0 = b * B;
   const int len = min(B, N - r0);
+  if (threadIdx.x == 0) nvalid = 0;
+  __syncthreads();
+  int mine = 0;
   for (int r = threadIdx.x; r < len; r += kPoolThreads) {
     int src = perm ? perm[r0 + r] : r0 + r;
-    if (src < 0 || src >= N) {  // a corrupt permutation is read as row 0 and flagged
+    if (src < -1 || src >= n_src) {  // a corrupt permutation entry is read as padding and flagged
       flag_error(status, PRISM_DEV_BAD_INDEX);
-      src = 0;
+      src = -1;
     }
     rows[r] = src;
+    mine += src >= 0;
   }
+  if (mine) atomicAdd(&nvalid, mine);
   __syncthreads();
   const int nvec = Hh * d / VW;
-  const float inv_len = 1.f / (float)len;
+  const float inv_len = nvalid > 0 ? 1.f / (float)nvalid : 0.f;
+  const R zero = {};
   for (int vi = threadIdx.x; vi < nvec; vi += kPoolThreads) {
     const int64_t col = (int64_t)vi * VW;
     float aq[VW], ak[VW];
@@ -86,10 +93,11 @@ __global__ void __launch_bounds__(kPoolThreads)
       R xq[4], xk[4], xv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int64_t src = (int64_t)rows[r + u] * ld + col;
-        xq[u] = *reinterpret_cast<const R*>(q + src);
-        xk[u] = *reinterpret_cast<const R*>(k + src);
-        if (vb) xv[u] = *reinterpret_cast<const R*>(v + src);
+        const int sr = rows[r + u];
+        const int64_t src = (int64_t)max(sr, 0) * ld + col;
+        xq[u] = sr >= 0 ? *reinterpret_cast<const R*>(q + src) : zero;
+        xk[u] = sr >= 0 ? *reinterpret_cast<const R*>(k + src) : zero;
+        if (vb) xv[u] = sr >= 0 ? *reinterpret_cast<const R*>(v + src) : zero;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -107,13 +115,14 @@ __global__ void __launch_bounds__(kPoolThreads)
       }
     }
     for (; r < len; ++r) {
-      const int64_t src = (int64_t)rows[r] * ld + col;
-      const R xq = *reinterpret_cast<const R*>(q + src);
-      const R xk = *reinterpret_cast<const R*>(k + src);
+      const int sr = rows[r];
+      const int64_t src = (int64_t)max(sr, 0) * ld + col;
+      const R xq = sr >= 0 ? *reinterpret_cast<const R*>(q + src) : zero;
+      const R xk = sr >= 0 ? *reinterpret_cast<const R*>(k + src) : zero;
       const int64_t dst = (int64_t)(r0 + r) * ldb + col;
       if (qb) *reinterpret_cast<R*>(qb + dst) = xq;
       if (kb) *reinterpret_cast<R*>(kb + dst) = xk;
-      if (vb) *reinterpret_cast<R*>(vb + dst) = *reinterpret_cast<const R*>(v + src);
+      if (vb) *reinterpret_cast<R*>(vb + dst) = sr >= 0 ? *reinterpret_cast<const R*>(v + src) : zero;
       float f[VW];
       Vec<T, VW>::to_f32(xq, f);
 #pragma unroll
@@ -238,13 +247,13 @@ __global__ void __launch_bounds__(kSThreads) scores_kernel(const float* __restri
 }
 
 template <typename T, int VW>
-cudaError_t launch_pool(const void* q, const void* k, const void* v, int64_t ld, const int32_t* perm, int N, int Hh,
-                        int d, int B, void* qb, void* kb, void* vb, int64_t ldb, float* qbar, float* kbar,
-                        cudaStream_t st, uint32_t* status) {
+cudaError_t launch_pool(const void* q, const void* k, const void* v, int64_t ld, const int32_t* perm, int n_src,
+                        int N, int Hh, int d, int B, void* qb, void* kb, void* vb, int64_t ldb, float* qbar,
+                        float* kbar, cudaStream_t st, uint32_t* status) {
   const int nb = (N + B - 1) / B;
   HookScope hs("pool_gather", st);
   pool_gather_kernel<T, VW><<<nb, kPoolThreads, (size_t)B * sizeof(int32_t), st>>>(
-      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), ld, perm, N, Hh, d, B,
+      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), ld, perm, n_src, N, Hh, d, B,
       static_cast<T*>(qb), static_cast<T*>(kb), static_cast<T*>(vb), ldb, qbar, kbar, nb, status);
   return cudaGetLastError();
 }
@@ -254,18 +263,18 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 }  // namespace
 
 cudaError_t pool_launch(const void* q, const void* k, const void* v, int dtype, int64_t ld, const int32_t* perm,
-                        int N, int Hh, int d, int B, void* qb, void* kb, void* vb, int64_t ldb, float* qbar,
-                        float* kbar, cudaStream_t st, uint32_t* status) {
+                        int n_src, int N, int Hh, int d, int B, void* qb, void* kb, void* vb, int64_t ldb,
+                        float* qbar, float* kbar, cudaStream_t st, uint32_t* status) {
   const bool ptr_ok = aligned16(q) && aligned16(k) && (!v || aligned16(v)) && (!qb || aligned16(qb)) &&
                       (!kb || aligned16(kb)) && (!vb || aligned16(vb));
   if (dtype == PRISM_BF16) {
     if (ptr_ok && d % 8 == 0 && ld % 8 == 0 && ldb % 8 == 0)
-      return launch_pool<__nv_bfloat16, 8>(q, k, v, ld, perm, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
-    return launch_pool<__nv_bfloat16, 1>(q, k, v, ld, perm, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
+      return launch_pool<__nv_bfloat16, 8>(q, k, v, ld, perm, n_src, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
+    return launch_pool<__nv_bfloat16, 1>(q, k, v, ld, perm, n_src, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
   }
   if (ptr_ok && d % 4 == 0 && ld % 4 == 0 && ldb % 4 == 0)
-    return launch_pool<float, 4>(q, k, v, ld, perm, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
-  return launch_pool<float, 1>(q, k, v, ld, perm, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
+    return launch_pool<float, 4>(q, k, v, ld, perm, n_src, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
+  return launch_pool<float, 1>(q, k, v, ld, perm, n_src, N, Hh, d, B, qb, kb, vb, ldb, qbar, kbar, st, status);
 }
 
 cudaError_t scores_launch(const float* qbar, const float* kbar, int Hh, int nb, int d, float* scores,

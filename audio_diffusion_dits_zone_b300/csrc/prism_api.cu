@@ -110,16 +110,18 @@ int check_attention_args(const void* q, const void* k, const void* v, int32_t dt
   return PRISM_OK;
 }
 
-// The tensor-core backward runs the fused kernel (dK, dV and dQ in one pass, dQ
-// reduce-added in fp32) unless PRISM_BWD_SPLIT=1 is set in the environment when the
-// library is first used: then the split kernels (dQ in its own pass, recomputing S
-// and dP), kept to compare the two designs.  Both compute the full gradients.
-bool split_backward() {
-  static const bool split = [] {
-    const char* v = std::getenv("PRISM_BWD_SPLIT");
+// The tensor-core backward runs the split kernels (dQ per query block, recomputing S
+// and dP; dK and dV per key block: seven tile products per kept pair, deterministic)
+// unless PRISM_BWD_FUSED=1 is set in the environment when the library is first used:
+// then the fused kernel (five products per pair, dQ reduce-added in fp32), which was
+// measured no faster on B300 and is kept to compare the two designs.  Both compute
+// the full gradients.
+bool fused_backward() {
+  static const bool fused = [] {
+    const char* v = std::getenv("PRISM_BWD_FUSED");
     return v && v[0] == '1';
   }();
-  return split;
+  return fused;
 }
 
 bool use_tc(int32_t dtype, int32_t d, int32_t B, int64_t ld, std::initializer_list<const void*> ptrs) {
@@ -238,11 +240,46 @@ int prism_zone_shapes_from_partials(const float* partials, int32_t n_parts, int3
   return e == cudaSuccess ? (launched(3), ok()) : cuda_fail(e, "prism_zone_shapes_from_partials");
 }
 
-int prism_pool_score(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld, const int32_t* perm,
-                     int32_t N, int32_t Hh, int32_t d, int32_t B, void* q_blk, void* k_blk, void* v_blk,
-                     int64_t ld_blk, float* qbar, float* kbar, float* scores, void* stream) {
+int prism_zone_chunked_size(int32_t T, int32_t H, int32_t W, int32_t zt, int32_t zh, int32_t zw, int32_t B,
+                            int32_t* nb, int64_t* np) {
+  prism::ZoneGeom g;
+  int rc;
+  if ((rc = zone_geometry(T, H, W, zt, zh, zw, &g)) != PRISM_OK) return rc;
+  if (B < 1) return fail(PRISM_EINVAL, "B must be >= 1");
+  if (!nb || !np) return fail(PRISM_EINVAL, "NULL pointer");
+  int64_t n = 0, p = 0;
+  prism::zone_chunked_size(g, B, &n, &p);
+  if (n > INT32_MAX || p > INT32_MAX) return fail(PRISM_EINVAL, "too many blocks");
+  *nb = (int32_t)n;
+  *np = p;
+  return ok();
+}
+
+int prism_zone_perm_chunked(const int32_t* zone_shape, int32_t T, int32_t H, int32_t W, int32_t zt, int32_t zh,
+                            int32_t zw, const int32_t* shapes, int32_t n_shapes, int32_t B, int32_t* perm_padded,
+                            int32_t* blen, void* ws, size_t* ws_bytes, void* stream) {
+  prism::ZoneGeom g;
+  prism::ShapeSet ss;
+  int rc;
+  if ((rc = shape_set(shapes, n_shapes, &ss)) != PRISM_OK) return rc;
+  if ((rc = zone_geometry(T, H, W, zt, zh, zw, &g)) != PRISM_OK) return rc;
+  if (B < 1) return fail(PRISM_EINVAL, "B must be >= 1");
+  int64_t nb = 0, np = 0;
+  prism::zone_chunked_size(g, B, &nb, &np);
+  if (np > INT32_MAX) return fail(PRISM_EINVAL, "too many blocks");
+  if (ws_query(ws, ws_bytes, ws_round((size_t)g.Z * sizeof(int32_t)), &rc)) return rc;
+  if (!zone_shape || !perm_padded || !blen) return fail(PRISM_EINVAL, "NULL pointer");
+  cudaError_t e = prism::zone_perm_chunked_launch(zone_shape, g, ss, B, perm_padded, blen, np, ws,
+                                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? (launched(3), ok()) : cuda_fail(e, "prism_zone_perm_chunked");
+}
+
+namespace {
+int pool_score_impl(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld, const int32_t* perm,
+                    int32_t n_src, int32_t N, int32_t Hh, int32_t d, int32_t B, void* q_blk, void* k_blk, void* v_blk,
+                    int64_t ld_blk, float* qbar, float* kbar, float* scores, void* stream, const char* name) {
   if (dtype != PRISM_F32 && dtype != PRISM_BF16) return fail(PRISM_EINVAL, "dtype invalid");
-  if (N < 1 || Hh < 1 || d < 1 || B < 1) return fail(PRISM_EINVAL, "sizes must be >= 1");
+  if (N < 1 || n_src < 1 || Hh < 1 || d < 1 || B < 1) return fail(PRISM_EINVAL, "sizes must be >= 1");
   if (d > 256) return fail(PRISM_EUNSUPPORTED, "d > 256");
   if (!q || !k) return fail(PRISM_EINVAL, "q and k must not be NULL");
   if (ld < (int64_t)Hh * d) return fail(PRISM_EINVAL, "ld < Hh * d");
@@ -255,12 +292,30 @@ int prism_pool_score(const void* q, const void* k, const void* v, int32_t dtype,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (qbar || kbar || copies)
-    e = prism::pool_launch(q, k, v, dtype, ld, perm, N, Hh, d, B, q_blk, k_blk, v_blk, copies ? ld_blk : ld, qbar,
-                           kbar, st, status_ptr());
+    e = prism::pool_launch(q, k, v, dtype, ld, perm, n_src, N, Hh, d, B, q_blk, k_blk, v_blk, copies ? ld_blk : ld,
+                           qbar, kbar, st, status_ptr());
   if (e == cudaSuccess && scores) e = prism::scores_launch(qbar, kbar, Hh, nb, d, scores, st);
-  if (e != cudaSuccess) return cuda_fail(e, "prism_pool_score");
+  if (e != cudaSuccess) return cuda_fail(e, name);
   launched((qbar || kbar || copies ? 1 : 0) + (scores ? 1 : 0));
   return ok();
+}
+}  // namespace
+
+int prism_pool_score(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld, const int32_t* perm,
+                     int32_t N, int32_t Hh, int32_t d, int32_t B, void* q_blk, void* k_blk, void* v_blk,
+                     int64_t ld_blk, float* qbar, float* kbar, float* scores, void* stream) {
+  return pool_score_impl(q, k, v, dtype, ld, perm, N, N, Hh, d, B, q_blk, k_blk, v_blk, ld_blk, qbar, kbar, scores,
+                         stream, "prism_pool_score");
+}
+
+int prism_pool_score_chunked(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld, int32_t n_src,
+                             const int32_t* perm_padded, int32_t np, int32_t Hh, int32_t d, int32_t B, void* q_blk,
+                             void* k_blk, void* v_blk, int64_t ld_blk, float* qbar, float* kbar, float* scores,
+                             void* stream) {
+  if (!perm_padded) return fail(PRISM_EINVAL, "perm_padded must not be NULL");
+  if (np % B != 0) return fail(PRISM_EINVAL, "np = %d is not a multiple of B = %d", np, B);
+  return pool_score_impl(q, k, v, dtype, ld, perm_padded, n_src, np, Hh, d, B, q_blk, k_blk, v_blk, ld_blk, qbar,
+                         kbar, scores, stream, "prism_pool_score_chunked");
 }
 
 int prism_select(const float* scores, int32_t Hh, int32_t nb, double sparsity, double cdf_tau, int32_t* counts,
@@ -296,7 +351,7 @@ int prism_score_select(const float* qbar, const float* kbar, int32_t Hh, int32_t
 
 int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32_t dtype, int64_t ld, int32_t N,
                   int32_t Hh, int32_t d, int32_t B, const int32_t* counts, const int32_t* idx, int32_t nb,
-                  void* o_blk, float* lse, void* ws, size_t* ws_bytes, void* stream) {
+                  const int32_t* blen, void* o_blk, float* lse, void* ws, size_t* ws_bytes, void* stream) {
   int rc = check_attention_args(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb);
   if (rc != PRISM_OK) return rc;
   if (ws_query(ws, ws_bytes, ws_round(0), &rc)) return rc;
@@ -304,9 +359,10 @@ int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (use_tc(dtype, d, B, ld, {q_blk, k_blk, v_blk, o_blk}))
-    e = prism::bsa_fwd_tc_launch(q_blk, k_blk, v_blk, ld, N, Hh, counts, idx, nb, o_blk, lse, st, status_ptr());
+    e = prism::bsa_fwd_tc_launch(q_blk, k_blk, v_blk, ld, N, Hh, counts, idx, nb, blen, o_blk, lse, st,
+                                 status_ptr());
   else
-    e = prism::bsa_fwd_simt_launch(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb, o_blk, lse, st,
+    e = prism::bsa_fwd_simt_launch(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb, blen, o_blk, lse, st,
                                    status_ptr());
   return e == cudaSuccess ? (launched(1), ok()) : cuda_fail(e, "prism_bsa_fwd");
 }
@@ -333,15 +389,15 @@ int prism_a2v_norm(const void* qv, const void* ka, const void* va, int32_t dtype
 
 int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk, const void* o_blk, const void* do_blk,
                   const float* lse, int32_t dtype, int64_t ld, int32_t N, int32_t Hh, int32_t d, int32_t B,
-                  const int32_t* counts, const int32_t* idx, int32_t nb, void* dq, void* dk, void* dv, void* ws,
-                  size_t* ws_bytes, void* stream) {
+                  const int32_t* counts, const int32_t* idx, int32_t nb, const int32_t* blen, void* dq, void* dk,
+                  void* dv, void* ws, size_t* ws_bytes, void* stream) {
   int rc = check_attention_args(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb);
   if (rc != PRISM_OK) return rc;
   // workspace: transposed lists | row statistics | (fused tensor-core path) fp32 dQ accumulator
   auto r256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t lists = r256(prism::lists_ws_bytes(Hh, nb));
   const bool tc = use_tc(dtype, d, B, ld, {q_blk, k_blk, v_blk, o_blk, do_blk, dq, dk, dv});
-  const bool fused = tc && !split_backward();
+  const bool fused = tc && fused_backward();
   const size_t rows = r256(tc ? prism::bwd_tc_rowstats_bytes(Hh, nb) : (size_t)Hh * N * sizeof(float));
   const size_t acc = fused ? prism::bwd_tc_dqacc_bytes(Hh, nb) : 0;
   if (ws_query(ws, ws_bytes, ws_round(lists + rows + acc), &rc)) return rc;
@@ -355,10 +411,10 @@ int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk, const
   if (e == cudaSuccess) {
     if (tc)
       e = prism::bsa_bwd_tc_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, ld, N, Hh, counts, idx, nb, dq, dk, dv,
-                                   tcounts, tidx, rowstats, dqacc, st, status_ptr());
+                                   tcounts, tidx, blen, rowstats, dqacc, st, status_ptr());
     else
       e = prism::bsa_bwd_simt_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, dtype, ld, N, Hh, d, B, counts, idx,
-                                     nb, dq, dk, dv, tcounts, tidx, rowstats, st, status_ptr());
+                                     nb, blen, dq, dk, dv, tcounts, tidx, rowstats, st, status_ptr());
   }
   return e == cudaSuccess ? (launched(5), ok()) : cuda_fail(e, "prism_bsa_bwd");
 }

@@ -14,9 +14,11 @@
 //
 // One CTA of R warps per (head, R consecutive query blocks):
 //   1. score rows: the R rows of qbar (transposed in shared memory) against every key
-//      block, 1024 keys per tile, kbar staged 8 channels at a time (double-buffered);
-//      a thread owns 4 rows x 8 keys (32 fp32 accumulators), so each channel step is
-//      three 16-byte shared loads for 32 FMAs.  The R score rows stay in shared memory.
+//      block, 512 keys per tile, kbar staged 8 channels at a time (double-buffered);
+//      a thread owns 4 rows x 4 keys (16 fp32 accumulators), so each channel step is
+//      two 16-byte shared loads for 16 FMAs, and two CTAs fit on an SM (one CTA's
+//      selection overlaps the other's score rows).  The R score rows stay in shared
+//      memory.
 //   2. selection: warp w selects row w.  Blocks are dropped into 256 equal-width
 //      buckets of [min, max] with fixed-point mass histograms; the scan from the top
 //      finds the bucket where both conditions are first met; everything above it is
@@ -33,7 +35,7 @@
 namespace prism {
 namespace {
 
-constexpr int kSsKeys = 1024;   // keys per score tile
+constexpr int kSsKeys = 512;    // keys per score tile
 constexpr int kSsSlice = 8;     // channels per staged slice of kbar
 constexpr int kBins = 256;
 constexpr int kCandCap = 256;   // candidates ranked exactly per level
@@ -307,7 +309,7 @@ __device__ int select_row(const float* sv, int nb, int k_top, double tau, uint8_
 }
 
 template <int R>
-__global__ void __launch_bounds__(32 * R) score_select_kernel(const float* __restrict__ qbar,
+__global__ void __launch_bounds__(32 * R, 2) score_select_kernel(const float* __restrict__ qbar,
                                                               const float* __restrict__ kbar, int nb, int d,
                                                               float scale, int k_top, double tau,
                                                               int32_t* __restrict__ counts,
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(32 * R) score_select_kernel(const float* __res
   }
   // ------------------------------------------------------------ score rows
   const int rg = tid >> 7;  // rows 4rg .. 4rg + 3
-  const int kg = tid & 127; // keys 8kg .. 8kg + 7 of the tile
+  const int kg = tid & 127; // keys 4kg .. 4kg + 3 of the tile
   constexpr int kPer = kSsKeys / kThreads;  // keys each thread stages per slice
   const int ns = d / kSsSlice;
   for (int k0 = 0; k0 < nb; k0 += kSsKeys) {
@@ -362,11 +364,11 @@ __global__ void __launch_bounds__(32 * R) score_select_kernel(const float* __res
         dst[7 * kSsKeys + jj] = st[u][1].w;
       }
     };
-    float acc[4][8];
+    float acc[4][4];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+      for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
     __syncthreads();  // qt written; the previous tile's readers of kt are done
     load(0);
     store(0);
@@ -378,30 +380,27 @@ __global__ void __launch_bounds__(32 * R) score_select_kernel(const float* __res
 #pragma unroll
       for (int dd = 0; dd < kSsSlice; ++dd) {
         const float4 a = *reinterpret_cast<const float4*>(qt + (size_t)(s * kSsSlice + dd) * R + 4 * rg);
-        const float4 b0 = *reinterpret_cast<const float4*>(kb + dd * kSsKeys + 8 * kg);
-        const float4 b1 = *reinterpret_cast<const float4*>(kb + dd * kSsKeys + 8 * kg + 4);
+        const float4 b = *reinterpret_cast<const float4*>(kb + dd * kSsKeys + 4 * kg);
         const float av[4] = {a.x, a.y, a.z, a.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-          for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+          for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
       }
       if (s + 1 < ns) store(buf ^ 1);
       __syncthreads();
     }
-    const int j0 = k0 + 8 * kg;
+    const int j0 = k0 + 4 * kg;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       float* row = S + (size_t)(4 * rg + r) * nbs;
-      if (j0 + 8 <= nb) {
+      if (j0 + 4 <= nb) {
         *reinterpret_cast<float4*>(row + j0) =
             make_float4(acc[r][0] * scale, acc[r][1] * scale, acc[r][2] * scale, acc[r][3] * scale);
-        *reinterpret_cast<float4*>(row + j0 + 4) =
-            make_float4(acc[r][4] * scale, acc[r][5] * scale, acc[r][6] * scale, acc[r][7] * scale);
       } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int c = 0; c < 4; ++c)
           if (j0 + c < nb) row[j0 + c] = acc[r][c] * scale;
       }
     }
@@ -445,7 +444,9 @@ cudaError_t score_select_launch(const float* qbar, const float* kbar, int Hh, in
   const float scale = 1.0f / sqrtf((float)d);
   cudaError_t e;
   const size_t s16 = score_select_smem<16>(nb, d);
-  if (s16 <= 232448) {
+  // 16-row CTAs while two of them fit on an SM, else 8-row CTAs (two or more per SM):
+  // one CTA's selection then overlaps another's score rows
+  if (2 * (s16 + 1024) <= 233472) {
     if ((e = cudaFuncSetAttribute(score_select_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s16)) !=
         cudaSuccess)
       return e;

@@ -17,10 +17,10 @@
 // Kernels (all HBM-bound or tiny):
 //   zone_tma       (bf16 features, zones up to 3 x 9 in t x h) persistent CTAs of 8
 //                  warps; each warp streams its own (zone, 64-channel) items as slabs of
-//                  4 w columns: one 4D TMA box [t][h][w][64 channels] per slab into a
-//                  double-buffered shared-memory stage, so the next slab is in flight
-//                  while this one is reduced (lane = 2 channels on packed fp32 pairs, all
-//                  line sums in registers, same arithmetic as zone_lines);
+//                  2 w columns: one 4D TMA box [t][h][w][64 channels] per slab into a
+//                  four-stage shared-memory ring, so three slabs are in flight while one
+//                  is reduced (lane = 2 channels on packed fp32 pairs, all line sums in
+//                  registers, same arithmetic as zone_lines);
 //   zone_lines     (zones up to 3 x 9 or 5 x 8 in t x h, even channel counts) one warp
 //                  per (zone, 64 channels), lane = 2 channels, so every load is one
 //                  128-byte run of a token row.  The warp streams the zone once,
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kLinesWarps * 32) zone_lines_kernel(const T* _
 constexpr int kTmaWarps = 8;
 constexpr int kSlabCh = 64;     // channels per slab: one 128-byte run of each token row, two per lane
 constexpr int kWq = 4;          // w columns per slab (a quarter of a 16-wide zone)
-constexpr int kTmaStages = 2;   // per warp
+constexpr int kTmaStages = 2;   // per warp: one slab in flight behind the one being reduced
 constexpr int kTmaMT = 3, kTmaMH = 9;  // slab extent along t and h (zones up to 3 x 9 in t x h)
 constexpr int kSlabBytes = kTmaMT * kTmaMH * kWq * kSlabCh * 2;  // 13,824 bytes
 
@@ -334,8 +334,8 @@ __device__ __forceinline__ void zone_slab_sums(const uint8_t* slab, int lane, f2
 // part[(z * nchunks + chunk) * 3 + a] exactly as zone_lines_kernel (chunk = 64 channels),
 // from slabs loaded with the 4D tensor map tm = feature viewed as [T][H][W][C] bf16 with
 // box {64, kWq, MH, MT}.  Persistent CTAs of kTmaWarps warps; each warp streams its own
-// items, nq slabs (w quarters) per item, through a two-stage ring that its lane 0 refills
-// (so the next slab is in flight while this one is reduced).  Zones that fill the box
+// items, nq slabs (kWq columns each) per item, through a kTmaStages-stage ring that its
+// lane 0 refills (so the next slabs are in flight while this one is reduced).  Zones that fill the box
 // take the unpredicated path; zones clipped by the grid (or smaller than the box) mask
 // the positions outside them, whose slab bytes are zero fill or a neighbour's tokens.
 template <int MT, int MH>
@@ -356,14 +356,14 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1)
   const int first = blockIdx.x * kTmaWarps + warp;
   const int nmine = first < items ? (items - first + stride - 1) / stride : 0;
   const int nslabs = nq * nmine;
-  auto issue = [&](int s) {  // slab s of this warp -> stage s & 1
+  auto issue = [&](int s) {  // slab s of this warp -> stage s % kTmaStages
     const int n = s / nq, q = s - n * nq;
     const int k = first + n * stride;
     const int z = k / nchunks, chunk = k - z * nchunks;
     const ZoneBox b = zone_box(g, z);
-    const uint32_t bar = smem_u32(&sm.full[warp][s & 1]);
+    const uint32_t bar = smem_u32(&sm.full[warp][s % kTmaStages]);
     mbar_arrive_expect_tx(bar, (uint32_t)(MT * MH * kWq * kSlabCh * 2));
-    tma_load_4d(smem_u32(sm.slab[warp][s & 1]), &tm, chunk * kSlabCh, b.w0 + q * kWq, b.h0, b.t0, bar);
+    tma_load_4d(smem_u32(sm.slab[warp][s % kTmaStages]), &tm, chunk * kSlabCh, b.w0 + q * kWq, b.h0, b.t0, bar);
   };
   int issued = 0;  // lane 0: slabs issued so far
   if (lane == 0) {
@@ -378,9 +378,10 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1)
     const int k = first + n * stride;
     const int z = k / nchunks, chunk = k - z * nchunks;
     const ZoneBox b = zone_box(g, z);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[warp][s & 1]), (s >> 1) & 1, &abort, status));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[warp][s % kTmaStages]),
+                                                      (s / kTmaStages) & 1, &abort, status));
     if (!ok) break;
-    const uint8_t* slab = sm.slab[warp][s & 1];
+    const uint8_t* slab = sm.slab[warp][s % kTmaStages];
     if (q == 0) {  // new item: reset the sums; shift by the zone's first token
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
@@ -430,10 +431,10 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1)
     }
   }
   // a warp that gave up waits (bounded) for the copies it still has in flight: the
-  // last slab issued into each stage completes that stage's phase (slab >> 1) & 1
+  // last slab issued into each stage completes that stage's phase (slab / stages) & 1
   if (abort && lane == 0)
     for (int s = issued - 1; s >= 0 && s >= issued - kTmaStages; --s)
-      drain_wait(smem_u32(&sm.full[warp][s & 1]), (s >> 1) & 1);
+      drain_wait(smem_u32(&sm.full[warp][s % kTmaStages]), (s / kTmaStages) & 1);
 }
 
 // stats[z * 8 + {0,1,2}] = v_a, {3,4,5} = u_a, 6 = zone mean of a2v.  The video term is
@@ -560,6 +561,72 @@ __global__ void zone_perm_kernel(ZoneGeom g, const int32_t* __restrict__ zone_sh
     const int64_t tile_off = (int64_t)tt * et * Lh * Lw + (int64_t)Et * th * eh * Lw + (int64_t)Et * Eh * tw * ew;
     const int within = ((lt - tt * et) * Eh + (lh - th * eh)) * Ew + (lw - tw * ew);
     perm[zone_off + tile_off + within] = (int32_t)n;
+  }
+}
+
+// Zone-chunked blocks: every zone's run of the block order cut into B-token blocks of
+// its own (the last one short).  One CTA: the blocks of each zone (ceil(tokens / B)),
+// their exclusive prefix over the zones in order (first[z]) and every block's length.
+__global__ void __launch_bounds__(1024) zone_chunk_blocks_kernel(ZoneGeom g, int B, int32_t* __restrict__ first,
+                                                                 int32_t* __restrict__ blen) {
+  __shared__ int32_t wsum[32];
+  __shared__ int32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int z0 = 0; z0 < g.Z; z0 += blockDim.x) {
+    const int z = z0 + threadIdx.x;
+    int n = 0, nblk = 0;
+    if (z < g.Z) {
+      const ZoneBox b = zone_box(g, z);
+      n = b.Lt * b.Lh * b.Lw;
+      nblk = (n + B - 1) / B;
+    }
+    int incl = nblk;  // inclusive scan of the CTA's zones
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = carry;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    const int f = before + incl - nblk;
+    if (z < g.Z) {
+      first[z] = f;
+      for (int m = 0; m < nblk; ++m) blen[f + m] = min(B, n - m * B);
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = before + incl;
+    __syncthreads();
+  }
+}
+
+__global__ void fill_i32_kernel(int32_t* __restrict__ p, int64_t n, int32_t v) {
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) p[e] = v;
+}
+
+// perm_padded[first[z] * B + position of the token in its zone] = raster token; the
+// in-zone position is the consecutive-chunk layout's (zone_perm_kernel).
+__global__ void zone_perm_chunked_kernel(ZoneGeom g, const int32_t* __restrict__ zone_shape, ShapeSet shapes, int B,
+                                         const int32_t* __restrict__ first, int32_t* __restrict__ perm) {
+  const int64_t N = (int64_t)g.T * g.H * g.W;
+  for (int64_t n = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; n < N; n += (int64_t)gridDim.x * blockDim.x) {
+    const int w = (int)(n % g.W);
+    const int h = (int)((n / g.W) % g.H);
+    const int t = (int)(n / ((int64_t)g.W * g.H));
+    const int zi_t = t / g.zt, zi_h = h / g.zh, zi_w = w / g.zw;
+    const int z = (zi_t * g.nzh + zi_h) * g.nzw + zi_w;
+    const int Lt = min(g.zt, g.T - zi_t * g.zt), Lh = min(g.zh, g.H - zi_h * g.zh), Lw = min(g.zw, g.W - zi_w * g.zw);
+    const int s = zone_shape[z];
+    const int et = shapes.e[s][0], eh = shapes.e[s][1], ew = shapes.e[s][2];
+    const int lt = t - zi_t * g.zt, lh = h - zi_h * g.zh, lw = w - zi_w * g.zw;
+    const int tt = lt / et, th = lh / eh, tw = lw / ew;
+    const int Et = min(et, Lt - tt * et), Eh = min(eh, Lh - th * eh), Ew = min(ew, Lw - tw * ew);
+    const int64_t tile_off = (int64_t)tt * et * Lh * Lw + (int64_t)Et * th * eh * Lw + (int64_t)Et * Eh * tw * ew;
+    const int within = ((lt - tt * et) * Eh + (lh - th * eh)) * Ew + (lw - tw * ew);
+    perm[(int64_t)first[z] * B + tile_off + within] = (int32_t)n;
   }
 }
 
@@ -745,6 +812,40 @@ cudaError_t zone_partials_launch(const void* feat, int dtype, int64_t ld, int C,
   if (e != cudaSuccess) return e;
   HookScope hs("zone_sum_chunks", st);
   zone_sum_chunks_kernel<<<(g.Z * 3 + 255) / 256, 256, 0, st>>>(part, nchunks, g.Z, out);
+  return cudaGetLastError();
+}
+
+void zone_chunked_size(const ZoneGeom& g, int B, int64_t* nb, int64_t* np) {
+  int64_t blocks = 0;
+  for (int zt = 0; zt < g.nzt; ++zt)
+    for (int zh = 0; zh < g.nzh; ++zh)
+      for (int zw = 0; zw < g.nzw; ++zw) {
+        const int64_t n = (int64_t)std::min(g.zt, g.T - zt * g.zt) * std::min(g.zh, g.H - zh * g.zh) *
+                          std::min(g.zw, g.W - zw * g.zw);
+        blocks += (n + B - 1) / B;
+      }
+  *nb = blocks;
+  *np = blocks * B;
+}
+
+cudaError_t zone_perm_chunked_launch(const int32_t* zone_shape, const ZoneGeom& g, const ShapeSet& shapes, int B,
+                                     int32_t* perm, int32_t* blen, int64_t np, void* ws, cudaStream_t st) {
+  int32_t* first = static_cast<int32_t*>(ws);
+  {
+    HookScope hs("zone_chunk_blocks", st);
+    zone_chunk_blocks_kernel<<<1, 1024, 0, st>>>(g, B, first, blen);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    HookScope hs("fill_padding", st);
+    fill_i32_kernel<<<(unsigned)std::min<int64_t>((np + 255) / 256, 148 * 16), 256, 0, st>>>(perm, np, -1);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t N = (int64_t)g.T * g.H * g.W;
+  HookScope hs("zone_perm_chunked", st);
+  zone_perm_chunked_kernel<<<(unsigned)std::min<int64_t>((N + 255) / 256, 148 * 16), 256, 0, st>>>(g, zone_shape,
+                                                                                               shapes, B, first, perm);
   return cudaGetLastError();
 }
 

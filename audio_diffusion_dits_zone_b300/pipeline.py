@@ -15,16 +15,24 @@ from . import synth
 class PrismLayer:
     """Device-resident state of one attention layer for a ``synth.Workload``."""
 
-    def __init__(self, wl: synth.Workload, device="cuda", sparsity=None, train=None, fused_select=False):
+    def __init__(self, wl: synth.Workload, device="cuda", sparsity=None, train=None, fused_select=False,
+                 chunked=False):
         """fused_select: block scores and selection in one call (prism_score_select), the
         score matrix never written; otherwise prism_pool_score writes the scores and
-        prism_select reads them."""
+        prism_select reads them.  chunked: zone-chunked blocks (every zone cut into B-token
+        blocks of its own, in a padded block order with per-block lengths) instead of
+        consecutive B-token chunks of the whole block order."""
         self.wl = wl
         self.fused_select = fused_select
+        self.chunked = chunked
         self.device = torch.device(device)
         self.sparsity = wl.sparsity if sparsity is None else sparsity
         self.train = (wl.mode == "fwd+bwd") if train is None else train
         N, Hh, d, nb = wl.N, wl.heads, wl.d, wl.nb
+        self.nrows = N  # rows of the block order (np for zone-chunked blocks)
+        if chunked:
+            nb, self.nrows = P.prism_zone_chunked_size(wl.grid, wl.zone, wl.block)
+        self.nb = nb
         dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
         self.dtype = dt
         e = dict(device=self.device)
@@ -36,22 +44,26 @@ class PrismLayer:
         self.a2v = torch.empty(N, dtype=torch.float32, **e)
         self.zone_shape = torch.empty(self.Z, dtype=torch.int32, **e)
         self.perm = torch.empty(N, dtype=torch.int32, **e)
-        self.q_blk = torch.empty_like(self.q)
-        self.k_blk = torch.empty_like(self.k)
-        self.v_blk = torch.empty_like(self.v)
+        self.perm_padded = torch.empty(self.nrows, dtype=torch.int32, **e) if chunked else None
+        self.blen = torch.empty(nb, dtype=torch.int32, **e) if chunked else None
+        self.ws_chunk = None
+        R = self.nrows
+        self.q_blk = torch.empty(R, Hh, d, dtype=dt, **e)
+        self.k_blk = torch.empty(R, Hh, d, dtype=dt, **e)
+        self.v_blk = torch.empty(R, Hh, d, dtype=dt, **e)
         self.qbar = torch.empty(Hh, nb, d, dtype=torch.float32, **e)
         self.kbar = torch.empty(Hh, nb, d, dtype=torch.float32, **e)
         self.scores = None if fused_select else torch.empty(Hh, nb, nb, dtype=torch.float32, **e)
         self.counts = torch.empty(Hh, nb, dtype=torch.int32, **e)
         self.idx = torch.empty(Hh, nb, nb, dtype=torch.int32, **e)
-        self.o_blk = torch.empty_like(self.q)
-        self.lse = torch.empty(Hh, N, dtype=torch.float32, **e)
+        self.o_blk = torch.empty_like(self.q_blk)
+        self.lse = torch.empty(Hh, R, dtype=torch.float32, **e)
         self.ws_zone = self.ws_fwd = self.ws_bwd = None
         if self.train:
-            self.do_blk = torch.empty_like(self.q)
-            self.dq = torch.empty_like(self.q)
-            self.dk = torch.empty_like(self.q)
-            self.dv = torch.empty_like(self.q)
+            self.do_blk = torch.empty_like(self.q_blk)
+            self.dq = torch.empty_like(self.q_blk)
+            self.dk = torch.empty_like(self.q_blk)
+            self.dv = torch.empty_like(self.q_blk)
 
     # ------------------------------------------------------------------ inputs
     def load_inputs(self, threads=8):
@@ -63,7 +75,8 @@ class PrismLayer:
         for tensor, dst in todo:
             for h0 in range(0, wl.heads, 8):   # groups of heads bound the host memory
                 heads = list(range(h0, min(h0 + 8, wl.heads)))
-                for h, x in zip(heads, synth.gen_heads(wl, tensor, heads, threads)):
+                rows = self.nrows if tensor == synth.DO_ID else 0
+                for h, x in zip(heads, synth.gen_heads(wl, tensor, heads, threads, rows)):
                     dst[:, h, :].copy_(torch.from_numpy(x).to(self.dtype))
         self.a2v.copy_(torch.from_numpy(synth.gen_a2v(wl)))
         torch.cuda.synchronize(self.device)
@@ -74,16 +87,25 @@ class PrismLayer:
         feat = self.v.view(wl.N, wl.heads * wl.d)
         self.ws_zone = P.prism_zone_shapes(feat, wl.heads * wl.d, self.a2v, wl.grid, wl.zone, wl.shapes,
                                            self.zone_shape, self.perm, self.ws_zone, stream)
+        if self.chunked:
+            self.ws_chunk = P.prism_zone_perm_chunked(self.zone_shape, wl.grid, wl.zone, wl.shapes, wl.block,
+                                                      self.perm_padded, self.blen, self.ws_chunk, stream)
+
+    def _pool(self, qbar, kbar, scores, stream):
+        if self.chunked:
+            P.prism_pool_score_chunked(self.q, self.k, self.v, self.perm_padded, self.wl.block, self.q_blk, self.k_blk,
+                                       self.v_blk, qbar, kbar, scores, stream)
+        else:
+            P.prism_pool_score(self.q, self.k, self.v, self.perm, self.wl.block, self.q_blk, self.k_blk, self.v_blk,
+                               qbar, kbar, scores, stream)
 
     def pool_score(self, stream=None):
-        P.prism_pool_score(self.q, self.k, self.v, self.perm, self.wl.block, self.q_blk, self.k_blk, self.v_blk,
-                           self.qbar, self.kbar, self.scores, stream)
+        self._pool(self.qbar, self.kbar, self.scores, stream)
 
     def pool_copies(self, stream=None):
         """Block-order copies of Q, K, V with the current permutation only (no means, no
         scores): what a step that reuses an earlier step's selection needs."""
-        P.prism_pool_score(self.q, self.k, self.v, self.perm, self.wl.block, self.q_blk, self.k_blk, self.v_blk,
-                           stream=stream)
+        self._pool(None, None, None, stream)
 
     def select(self, stream=None):
         if self.fused_select:
@@ -100,7 +122,7 @@ class PrismLayer:
         for h0, h1 in self._groups():
             self.ws_fwd = P.prism_bsa_fwd(self.q_blk[:, h0:h1], self.k_blk[:, h0:h1], self.v_blk[:, h0:h1], B,
                                           self.counts[h0:h1], self.idx[h0:h1], self.o_blk[:, h0:h1],
-                                          self.lse[h0:h1], self.ws_fwd, stream)
+                                          self.lse[h0:h1], self.ws_fwd, stream, blen=self.blen)
 
     def attention_bwd(self, stream=None):
         B = self.wl.block
@@ -108,7 +130,7 @@ class PrismLayer:
             self.ws_bwd = P.prism_bsa_bwd(self.q_blk[:, h0:h1], self.k_blk[:, h0:h1], self.v_blk[:, h0:h1],
                                           self.o_blk[:, h0:h1], self.do_blk[:, h0:h1], self.lse[h0:h1], B,
                                           self.counts[h0:h1], self.idx[h0:h1], self.dq[:, h0:h1],
-                                          self.dk[:, h0:h1], self.dv[:, h0:h1], self.ws_bwd, stream)
+                                          self.dk[:, h0:h1], self.dv[:, h0:h1], self.ws_bwd, stream, blen=self.blen)
 
     def forward(self, stream=None):
         self.zone_shapes(stream)
@@ -123,14 +145,21 @@ class PrismLayer:
             self.attention_bwd(stream)
 
     # ------------------------------------------------------------------- work
-    def executed_pairs(self) -> np.ndarray:
-        """Per (head, query block): sum over kept blocks of |b_i| * |b_j| (token pairs)."""
+    def block_lengths(self):
+        """Tokens of every block (int64 device tensor)."""
         wl = self.wl
+        if self.chunked:
+            return self.blen.long()
         lens = torch.full((wl.nb,), wl.block, dtype=torch.int64, device=self.device)
         lens[-1] = wl.N - wl.block * (wl.nb - 1)
-        nbr = torch.arange(wl.nb, device=self.device)
+        return lens
+
+    def executed_pairs(self) -> np.ndarray:
+        """Per (head, query block): sum over kept blocks of |b_i| * |b_j| (token pairs)."""
+        lens = self.block_lengths()
+        nbr = torch.arange(self.nb, device=self.device)
         valid = nbr[None, None, :] < self.counts[:, :, None].long()
-        jl = lens[self.idx.long().clamp(0, wl.nb - 1)] * valid
+        jl = lens[self.idx.long().clamp(0, self.nb - 1)] * valid
         return (jl.sum(-1) * lens[None, :]).cpu().numpy()
 
     def flops(self):

@@ -32,9 +32,14 @@ _SIGS = {
     "prism_pool_score": [_P, _P, _P, _I32, _I64, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _P, _P, _P, _P],
     "prism_select": [_P, _I32, _I32, ctypes.c_double, ctypes.c_double, _P, _P, _P],
     "prism_score_select": [_P, _P, _I32, _I32, _I32, ctypes.c_double, ctypes.c_double, _P, _P, _P],
-    "prism_bsa_fwd": [_P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P],
-    "prism_bsa_bwd": [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _P, _SZ,
-                      _P],
+    "prism_bsa_fwd": [_P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P],
+    "prism_bsa_bwd": [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _I32, _P, _P, _P, _P, _P,
+                      _SZ, _P],
+    "prism_pool_score_chunked": [_P, _P, _P, _I32, _I64, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _I64, _P, _P,
+                                 _P, _P],
+    "prism_zone_chunked_size": [_I32, _I32, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(ctypes.c_int32),
+                                ctypes.POINTER(ctypes.c_int64)],
+    "prism_zone_perm_chunked": [_P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P, _SZ, _P],
     "prism_a2v_norm": [_P, _P, _P, _I32, _I64, _I64, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
     "prism_attn_mse": [_P, _P, _I32, _I64, _I32, _I32, _I32, _P, _P, _SZ, _P],
     "prism_status_check": [_P, ctypes.POINTER(ctypes.c_uint32)],
@@ -245,6 +250,39 @@ def prism_zone_shapes_from_partials(partials, C_total, a2v, grid, zone, shapes, 
     return ws
 
 
+def prism_zone_chunked_size(grid, zone, B):
+    """(nb, np): blocks and padded length of the zone-chunked block order (host only)."""
+    nb, np_ = ctypes.c_int32(0), ctypes.c_int64(0)
+    _check(lib().prism_zone_chunked_size(*grid, *zone, B, ctypes.byref(nb), ctypes.byref(np_)))
+    return nb.value, np_.value
+
+
+def prism_zone_perm_chunked(zone_shape, grid, zone, shapes, B, perm_padded, blen, ws=None, stream=None):
+    """Padded zone-chunked block order (-1 at padding) and block lengths from zone shapes."""
+    sh = (ctypes.c_int32 * (3 * len(shapes)))(*[int(e) for s in shapes for e in s])
+    st = _stream(stream)
+
+    def call(wsp, nbytes):
+        return lib().prism_zone_perm_chunked(_ptr(zone_shape), *grid, *zone, sh, len(shapes), B, _ptr(perm_padded),
+                                             _ptr(blen), wsp, nbytes, st)
+
+    ws, nbytes = _ws(call, ws, zone_shape.device)
+    _check(call(_ptr(ws), ctypes.byref(nbytes)))
+    return ws
+
+
+def prism_pool_score_chunked(q, k, v, perm_padded, B, q_blk=None, k_blk=None, v_blk=None, qbar=None, kbar=None,
+                             scores=None, stream=None):
+    """prism_pool_score over the padded zone-chunked block order; q, k, v: [n_src, Hh, d]."""
+    n_src, Hh, d = q.shape
+    np_ = perm_padded.numel()
+    ldb = _ld(q_blk) if q_blk is not None else (_ld(k_blk) if k_blk is not None else
+                                                (_ld(v_blk) if v_blk is not None else 0))
+    _check(lib().prism_pool_score_chunked(_ptr(q), _ptr(k), _ptr(v), _dtype(q), _ld(q), n_src, _ptr(perm_padded),
+                                          np_, Hh, d, B, _ptr(q_blk), _ptr(k_blk), _ptr(v_blk), ldb, _ptr(qbar),
+                                          _ptr(kbar), _ptr(scores), _stream(stream)))
+
+
 # ------------------------------------------------------------------- step 2
 def prism_pool_score(q, k, v, perm, B, q_blk=None, k_blk=None, v_blk=None, qbar=None, kbar=None, scores=None,
                      stream=None):
@@ -275,15 +313,16 @@ def prism_score_select(qbar, kbar, sparsity, cdf_tau, counts, idx, stream=None):
 
 
 # ------------------------------------------------------------------- step 4
-def prism_bsa_fwd(q_blk, k_blk, v_blk, B, counts, idx, o_blk, lse, ws=None, stream=None):
-    """Block-sparse attention forward.  Returns the workspace tensor it used."""
+def prism_bsa_fwd(q_blk, k_blk, v_blk, B, counts, idx, o_blk, lse, ws=None, stream=None, blen=None):
+    """Block-sparse attention forward.  blen: per-block token counts of zone-chunked
+    blocks (padded block order), or None.  Returns the workspace tensor it used."""
     N, Hh, d = q_blk.shape
     nb = -(-N // B)
     st = _stream(stream)
 
     def call(wsp, nbytes):
         return lib().prism_bsa_fwd(_ptr(q_blk), _ptr(k_blk), _ptr(v_blk), _dtype(q_blk), _ld(q_blk), N, Hh, d, B,
-                                   _ptr(counts), _ptr(idx), nb, _ptr(o_blk), _ptr(lse), wsp, nbytes, st)
+                                   _ptr(counts), _ptr(idx), nb, _ptr(blen), _ptr(o_blk), _ptr(lse), wsp, nbytes, st)
 
     ws, nbytes = _ws(call, ws, q_blk.device)
     _check(call(_ptr(ws), ctypes.byref(nbytes)))
@@ -310,16 +349,18 @@ def prism_a2v_norm(qv, ka, va, a2v, o=None, ws=None, stream=None):
 
 
 # ------------------------------------------------------------------- step 5
-def prism_bsa_bwd(q_blk, k_blk, v_blk, o_blk, do_blk, lse, B, counts, idx, dq, dk, dv, ws=None, stream=None):
-    """Block-sparse attention backward.  Returns the workspace tensor it used."""
+def prism_bsa_bwd(q_blk, k_blk, v_blk, o_blk, do_blk, lse, B, counts, idx, dq, dk, dv, ws=None, stream=None,
+                  blen=None):
+    """Block-sparse attention backward (blen as prism_bsa_fwd).  Returns the workspace
+    tensor it used."""
     N, Hh, d = q_blk.shape
     nb = -(-N // B)
     st = _stream(stream)
 
     def call(wsp, nbytes):
         return lib().prism_bsa_bwd(_ptr(q_blk), _ptr(k_blk), _ptr(v_blk), _ptr(o_blk), _ptr(do_blk), _ptr(lse),
-                                   _dtype(q_blk), _ld(q_blk), N, Hh, d, B, _ptr(counts), _ptr(idx), nb, _ptr(dq),
-                                   _ptr(dk), _ptr(dv), wsp, nbytes, st)
+                                   _dtype(q_blk), _ld(q_blk), N, Hh, d, B, _ptr(counts), _ptr(idx), nb, _ptr(blen),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), wsp, nbytes, st)
 
     ws, nbytes = _ws(call, ws, q_blk.device)
     _check(call(_ptr(ws), ctypes.byref(nbytes)))

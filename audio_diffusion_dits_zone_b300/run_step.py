@@ -20,9 +20,12 @@ def main():
     ap.add_argument("--workload", default="720p-4h", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--sparsity", type=float, default=None)
+    ap.add_argument("--select", default="split", choices=["fused", "split"])
+    ap.add_argument("--blocks", default="consecutive", choices=["consecutive", "zone-chunked"])
     a = ap.parse_args()
     wl = synth.WORKLOADS[a.workload]
-    layer = PrismLayer(wl, "cuda", sparsity=a.sparsity)
+    layer = PrismLayer(wl, "cuda", sparsity=a.sparsity, fused_select=a.select == "fused",
+                       chunked=a.blocks == "zone-chunked")
     layer.load_inputs()
     n0 = P.launch_count()
     for _ in range(a.steps):

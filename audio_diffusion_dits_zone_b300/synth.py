@@ -102,6 +102,10 @@ WORKLOADS = {
     # the 720p training layer with 4 heads: a small case of the same kernels for profiling
     "720p-4h": Workload("720p-4h", 5, (21, 45, 80), 4, 128, "bf16", (3, 9, 16), 128, SHAPES_128,
                         0.80, 0.20, 1, 3.0, (44, 42, 42), "fwd+bwd"),
+    # the 2K forward layer with 4 heads (2,363 blocks per row): the profiling case of the
+    # selection kernels at that row length
+    "2k-4h": Workload("2k-4h", 6, (21, 90, 160), 4, 128, "bf16", (3, 9, 16), 128, SHAPES_128,
+                      0.93, 0.20, 3, 6.0, (44, 42, 42), "fwd"),
 }
 
 
@@ -217,9 +221,10 @@ def trajectory_blend(clean: np.ndarray, noise: np.ndarray, t: int, n_steps: int)
     return (np.float32(1.0) - sg) * clean + sg * noise
 
 
-def gen_do_head(wl: Workload, head: int) -> np.ndarray:
-    """One head of the upstream gradient dO ~ N(0,1), float32 [N, d] (block order)."""
-    return _rng(wl.cid, DO_ID, head).standard_normal((wl.N, wl.d), dtype=np.float32)
+def gen_do_head(wl: Workload, head: int, rows: int = 0) -> np.ndarray:
+    """One head of the upstream gradient dO ~ N(0,1), float32 [rows or N, d] (block order;
+    rows > N for a padded block order)."""
+    return _rng(wl.cid, DO_ID, head).standard_normal((rows or wl.N, wl.d), dtype=np.float32)
 
 
 def gen_a2v(wl: Workload) -> np.ndarray:
@@ -247,12 +252,13 @@ def round_inputs(wl: Workload, x: np.ndarray) -> np.ndarray:
     return to_bf16(x) if wl.dtype == "bf16" else np.asarray(x, dtype=np.float32)
 
 
-def gen_heads(wl: Workload, tensor: int, heads, threads: int = 8) -> list:
-    """Several heads of one tensor, generated in parallel threads (numpy releases the GIL)."""
+def gen_heads(wl: Workload, tensor: int, heads, threads: int = 8, rows: int = 0) -> list:
+    """Several heads of one tensor, generated in parallel threads (numpy releases the GIL).
+    rows: the block-order length of dO when it is not N (a padded block order)."""
     rope = rope_tables(wl.grid, wl.d, wl.rope_split) if tensor in (Q_ID, K_ID) else None
 
     def one(h):
-        x = gen_do_head(wl, h) if tensor == DO_ID else gen_head(wl, tensor, h, rope)
+        x = gen_do_head(wl, h, rows) if tensor == DO_ID else gen_head(wl, tensor, h, rope)
         return round_inputs(wl, x)
 
     with ThreadPoolExecutor(max_workers=threads) as ex:

@@ -176,7 +176,8 @@ def run_ours(args, rank, world, local_rank):
     wl = synth.WORKLOADS[args.workload]
     sp = wl.sparsity if args.sparsity is None else args.sparsity
     train = wl.mode == "fwd+bwd"
-    layer = PrismLayer(wl, dev, sparsity=sp, train=train, fused_select=args.select == "fused")
+    layer = PrismLayer(wl, dev, sparsity=sp, train=train, fused_select=args.select == "fused",
+                       chunked=args.blocks == "zone-chunked")
     layer.load_inputs()
     layer.step()
     if P.status_check() != 0:
@@ -230,17 +231,17 @@ def run_ours(args, rank, world, local_rank):
     pairs = fwd_fl / (4.0 * wl.d)
     C = wl.heads * wl.d
     kept = int(layer.counts.sum().item())
-    npad = wl.nb * wl.block
+    nb, R = layer.nb, layer.nrows
     algo = {
         "bsa_fwd_tc": ("tensor", 4.0 * pairs * wl.d), "bsa_dq_tc": ("tensor", 6.0 * pairs * wl.d),
         "bsa_dkdv_tc": ("tensor", 8.0 * pairs * wl.d), "bsa_bwd_tc": ("tensor", 10.0 * pairs * wl.d),
-        "dq_convert": ("hbm", wl.heads * npad * wl.d * 4.0 + wl.N * C * 2.0),
+        "dq_convert": ("hbm", wl.heads * R * wl.d * 4.0 + R * C * 2.0),
         "zone_tma": ("hbm", wl.N * C * 2.0), "zone_partial": ("hbm", wl.N * C * 2.0),
-        "pool_gather": ("hbm", 6.0 * wl.N * C * 2 + 2.0 * wl.heads * wl.nb * wl.d * 4),
-        "scores": ("hbm", wl.heads * wl.nb ** 2 * 4.0 + 2.0 * wl.heads * wl.nb * wl.d * 4),
-        "score_select": ("hbm", 2.0 * wl.heads * wl.nb * wl.d * 4 + wl.heads * wl.nb * 4 + 4.0 * kept),
-        "select": ("hbm", wl.heads * wl.nb ** 2 * 4.0 + wl.heads * wl.nb * 4 + 4.0 * kept),
-        "bwd_prep": ("hbm", 2.0 * wl.N * C * 2 + wl.heads * wl.N * 4 + 2.0 * wl.heads * wl.nb * wl.block * 4),
+        "pool_gather": ("hbm", 3.0 * wl.N * C * 2 + 3.0 * R * C * 2 + 2.0 * wl.heads * nb * wl.d * 4),
+        "scores": ("hbm", wl.heads * nb ** 2 * 4.0 + 2.0 * wl.heads * nb * wl.d * 4),
+        "score_select": ("hbm", 2.0 * wl.heads * nb * wl.d * 4 + wl.heads * nb * 4 + 4.0 * kept),
+        "select": ("hbm", wl.heads * nb ** 2 * 4.0 + wl.heads * nb * 4 + 4.0 * kept),
+        "bwd_prep": ("hbm", 2.0 * R * C * 2 + wl.heads * R * 4 + 2.0 * wl.heads * nb * wl.block * 4),
     }
     for n, (bound, w) in algo.items():
         if n in per_kernel:
@@ -252,6 +253,23 @@ def run_ours(args, rank, world, local_rank):
             else:
                 per_kernel[n]["GB/s"] = round(w / t / 1e9, 1)
                 per_kernel[n]["frac_hbm"] = round(w / t / 1e9 / pk["hbm_gbs"], 4)
+    # the score GEMM on CUDA cores against the fp32 FMA peak: SMs x 128 lanes x 2 FLOP x clock
+    # (the maximum SM clock, and the median one sampled under load)
+    clocks = clk.summary()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    score_flops = 2.0 * wl.heads * nb ** 2 * wl.d
+    for n in ("scores", "score_select"):
+        if n in per_kernel:
+            t = per_kernel[n]["ms_per_step"] * 1e-3
+            achieved = score_flops / t / 1e12
+            per_kernel[n]["fp32_TFLOP/s"] = round(achieved, 2)
+            if clocks.get("sm_max_mhz"):
+                peak_max = sms * 128 * 2 * clocks["sm_max_mhz"] * 1e6 / 1e12
+                per_kernel[n]["frac_fp32_alu"] = round(achieved / peak_max, 4)
+                per_kernel[n]["fp32_alu_peak"] = f"{peak_max:.1f} TFLOP/s at {clocks['sm_max_mhz']:.0f} MHz"
+            if clocks.get("sm_mhz"):
+                per_kernel[n]["frac_fp32_alu_at_median_clock"] = round(
+                    achieved / (sms * 128 * 2 * clocks["sm_mhz"] * 1e6 / 1e12), 4)
     dom = max(per_kernel, key=lambda n: per_kernel[n]["ms_per_step"])
     bound, w = algo.get(dom, ("tensor", 0.0))
     t_launch = per_kernel[dom]["ms_per_launch"] * 1e-3
@@ -278,7 +296,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Wan-VAE-shaped latents, no weights)",
-        "config": workload_config(wl, sp),
+        "config": {**workload_config(wl, sp), "blocks": args.blocks, "select": args.select,
+                   "backward": "fused" if os.environ.get("PRISM_BWD_FUSED") == "1" else "split"},
         "ms_per_layer": round(ms, 3),
         "tflops_executed": round(work / (ms * 1e-3) / 1e12, 3),
         "tflops_dense_equivalent": round((dense_f + dense_b) / (ms * 1e-3) / 1e12, 3),
@@ -288,11 +307,11 @@ def run_ours(args, rank, world, local_rank):
         "per_kernel": per_kernel,
         "attention_tflops": {"bsa_fwd": round(fwd_fl / (per_call["bsa_fwd"] * 1e-3) / 1e12, 2),
                              **({"bsa_bwd": round(bwd_fl / (per_call["bsa_bwd"] * 1e-3) / 1e12, 2)} if train else {})},
-        "kept_fraction": round(float(layer.counts.double().mean().item()) / wl.nb, 4),
+        "kept_fraction": round(float(layer.counts.double().mean().item()) / layer.nb, 4),
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, sp, budget_s=args.cpu_seconds)
@@ -771,6 +790,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (extra workloads)")
     ap.add_argument("--select", default="split", choices=["fused", "split"],
                     help="block scores + selection in one kernel (fused) or scores written, then selection (split)")
+    ap.add_argument("--blocks", default="consecutive", choices=["consecutive", "zone-chunked"],
+                    help="blocks as consecutive B-token chunks of the block order, or cut per zone")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -125,6 +125,34 @@ int prism_zone_shapes_from_partials(const float* partials, int32_t n_parts, int3
                                     void* ws, size_t* ws_bytes, void* stream);
 
 /*
+ * Zone-chunked blocks -- the other reading of the block construction (Prism page,
+ * "Region-adapted block construction", paragraph 1: blocks are built per macro-zone):
+ * instead of cutting the whole block order into consecutive B-token blocks (a block
+ * may then span the end of one zone and the start of the next), every zone's run of
+ * the block order is cut into B-token blocks of its own, the last one short, so that
+ * no block holds tokens of two zones.  Same token order as prism_zone_shapes' perm.
+ * The blocks are laid out in a padded block order: each zone's run is followed by
+ * padding up to a multiple of B, so block b is positions [b*B, (b+1)*B) and holds
+ * blen[b] tokens at its start.  The other calls take this layout with N = np and
+ * nb = np / B: prism_pool_score reads perm entries -1 as padding, and the attention
+ * calls take blen.
+ *
+ * prism_zone_chunked_size -- host only: nb (blocks) and np = nb * B for the grid,
+ *   zone extents and B.
+ * prism_zone_perm_chunked -- from zone_shape (prism_zone_shapes' output):
+ *   perm_padded out [np] int32: raster token at each padded position, -1 at padding;
+ *   blen out [nb] int32: tokens of each block (1 .. B).
+ *   ws: workspace (NULL = size query): one int32 per zone.
+ */
+int prism_zone_chunked_size(int32_t T, int32_t H, int32_t W, int32_t zt, int32_t zh, int32_t zw,
+                            int32_t B, int32_t* nb, int64_t* np);
+int prism_zone_perm_chunked(const int32_t* zone_shape, int32_t T, int32_t H, int32_t W,
+                            int32_t zt, int32_t zh, int32_t zw,
+                            const int32_t* shapes, int32_t n_shapes, int32_t B,
+                            int32_t* perm_padded, int32_t* blen,
+                            void* ws, size_t* ws_bytes, void* stream);
+
+/*
  * prism_zone_shapes_noalloc -- the same computation and outputs as
  * prism_zone_shapes, for callers that cannot give the library device memory (their
  * device memory belongs to another allocator, or they run in a hook that must not
@@ -137,6 +165,18 @@ int prism_zone_shapes_from_partials(const float* partials, int32_t n_parts, int3
  * call before any stream capture).  All calls on a device share the array: calls
  * that overlap on the GPU race and must be ordered by the caller.  Allocates nothing.
  */
+/*
+ * prism_pool_score_chunked -- prism_pool_score for zone-chunked blocks: q, k, v are the
+ * n_src raster rows; perm_padded [np] (prism_zone_perm_chunked) gives the block order
+ * with -1 at padding positions, whose rows of the copies are written as zeros and are
+ * not counted in the block means (each mean is over the block's blen tokens).
+ * np must be a multiple of B; the other arguments as prism_pool_score with N = np.
+ */
+int prism_pool_score_chunked(const void* q, const void* k, const void* v, int32_t dtype, int64_t ld,
+                             int32_t n_src, const int32_t* perm_padded, int32_t np, int32_t Hh,
+                             int32_t d, int32_t B, void* q_blk, void* k_blk, void* v_blk,
+                             int64_t ld_blk, float* qbar, float* kbar, float* scores, void* stream);
+
 int prism_zone_shapes_noalloc(const void* feat, int32_t feat_dtype, int64_t feat_ld, int32_t C,
                               const float* a2v, int32_t T, int32_t H, int32_t W,
                               int32_t zt, int32_t zh, int32_t zw,
@@ -210,6 +250,11 @@ int prism_score_select(const float* qbar, const float* kbar, int32_t Hh, int32_t
  *         PRISM_F32 (CUDA-core path).
  * counts  [Hh][nb] int32;  idx [Hh][nb][nb] int32 (row stride nb), nb = ceil(N/B).
  *         Entries outside [0, nb) are skipped and flagged PRISM_DEV_BAD_INDEX.
+ * blen    NULL (blocks are the B-token chunks of the block order, the last one short),
+ *         or [nb] int32 for zone-chunked blocks in the padded block order
+ *         (prism_zone_perm_chunked; N = nb * B): block b holds its first blen[b] rows;
+ *         the other rows are padding, neither queries nor keys (their O and lse rows
+ *         are unspecified).
  * o_blk   out [N][Hh][d], row stride ld, same dtype as the inputs.
  * lse     out [Hh][N] fp32 (natural log).
  * ws      workspace (NULL = size query).
@@ -217,7 +262,7 @@ int prism_score_select(const float* qbar, const float* kbar, int32_t Hh, int32_t
  */
 int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32_t dtype,
                   int64_t ld, int32_t N, int32_t Hh, int32_t d, int32_t B,
-                  const int32_t* counts, const int32_t* idx, int32_t nb,
+                  const int32_t* counts, const int32_t* idx, int32_t nb, const int32_t* blen,
                   void* o_blk, float* lse, void* ws, size_t* ws_bytes, void* stream);
 
 /*
@@ -253,6 +298,7 @@ int prism_a2v_norm(const void* qv, const void* ka, const void* va, int32_t dtype
  *
  * q_blk .. do_blk  [N][Hh][d] block order, row stride ld, dtype as in the forward.
  * lse     [Hh][N] fp32 from prism_bsa_fwd.
+ * blen    as prism_bsa_fwd (padding rows get zero gradients; their dO rows are ignored).
  * dq, dk, dv  out [N][Hh][d], row stride ld, same dtype.
  * ws      workspace (NULL = size query): transposed lists and row statistics.
  * Limits as prism_bsa_fwd.
@@ -260,7 +306,7 @@ int prism_a2v_norm(const void* qv, const void* ka, const void* va, int32_t dtype
 int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk,
                   const void* o_blk, const void* do_blk, const float* lse, int32_t dtype,
                   int64_t ld, int32_t N, int32_t Hh, int32_t d, int32_t B,
-                  const int32_t* counts, const int32_t* idx, int32_t nb,
+                  const int32_t* counts, const int32_t* idx, int32_t nb, const int32_t* blen,
                   void* dq, void* dk, void* dv, void* ws, size_t* ws_bytes, void* stream);
 
 /*

@@ -61,29 +61,29 @@ def test_select_rejects_bad_arguments(L):
 def test_attention_rejects_bad_arguments(L):
     p = ctypes.c_void_p(256)
     # wrong nb
-    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 1024, 1000, 8, 128, 128, p, p, 7, p, p, None, _sz(), None) == \
+    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 1024, 1000, 8, 128, 128, p, p, 7, None, p, p, None, _sz(), None) == \
         P.PRISM_EINVAL
     # unsupported head dim / block size
-    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 1024, 1000, 8, 96, 128, p, p, 8, p, p, None, _sz(), None) == \
+    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 1024, 1000, 8, 96, 128, p, p, 8, None, p, p, None, _sz(), None) == \
         P.PRISM_EUNSUPPORTED
-    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 1024, 1000, 8, 128, 32, p, p, 32, p, p, None, _sz(), None) == \
+    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 1024, 1000, 8, 128, 32, p, p, 32, None, p, p, None, _sz(), None) == \
         P.PRISM_EUNSUPPORTED
     # ld too small
-    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 512, 1000, 8, 128, 128, p, p, 8, p, p, None, _sz(), None) == \
+    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 512, 1000, 8, 128, 128, p, p, 8, None, p, p, None, _sz(), None) == \
         P.PRISM_EINVAL
     # bad dtype
-    assert L.prism_bsa_bwd(p, p, p, p, p, p, 7, 1024, 1000, 8, 128, 128, p, p, 8, p, p, p, None, _sz(), None) == \
+    assert L.prism_bsa_bwd(p, p, p, p, p, p, 7, 1024, 1000, 8, 128, 128, p, p, 8, None, p, p, p, None, _sz(), None) == \
         P.PRISM_EINVAL
 
 
 def test_workspace_query_needs_no_gpu(L):
     p = ctypes.c_void_p(256)
     n = ctypes.c_size_t(0)
-    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 1024, 1000, 8, 128, 128, p, p, 8, p, p, None, ctypes.byref(n),
+    assert L.prism_bsa_fwd(p, p, p, P.PRISM_BF16, 1024, 1000, 8, 128, 128, p, p, 8, None, p, p, None, ctypes.byref(n),
                            None) == P.PRISM_OK
     assert n.value >= 256 and n.value % 256 == 0
     m = ctypes.c_size_t(0)
-    assert L.prism_bsa_bwd(p, p, p, p, p, p, P.PRISM_BF16, 1024, 1000, 8, 128, 128, p, p, 8, p, p, p, None,
+    assert L.prism_bsa_bwd(p, p, p, p, p, p, P.PRISM_BF16, 1024, 1000, 8, 128, 128, p, p, 8, None, p, p, p, None,
                            ctypes.byref(m), None) == P.PRISM_OK
     # transposed lists (bits + counts + indices) and the row term D
     assert m.value >= 8 * 8 * 8 * 4 + 8 * 1000 * 4
@@ -133,3 +133,23 @@ def test_a2v_norm_argument_rules_and_workspace(L):
     assert L.prism_a2v_norm(ctypes.c_void_p(258), p, p, P.PRISM_BF16, 5120, 5120, 75600, 157, 40, 128, None, p, ws,
                             ctypes.byref(big), None) == P.PRISM_EINVAL
     assert b"aligned" in L.prism_last_error()
+
+
+def test_zone_chunked_sizes_closed_form(L):
+    # host only: 720p: 175 zones of 432 tokens, 4 blocks each; 1080p: 7 planes of
+    # 49 x 4 + 7 x 2 + 7 x 2 + 1 blocks (zones clipped to 5 rows / 8 columns at the edges)
+    nb, np_ = ctypes.c_int32(0), ctypes.c_int64(0)
+    assert L.prism_zone_chunked_size(21, 45, 80, 3, 9, 16, 128, ctypes.byref(nb), ctypes.byref(np_)) == P.PRISM_OK
+    assert (nb.value, np_.value) == (700, 700 * 128)
+    assert L.prism_zone_chunked_size(21, 68, 120, 3, 9, 16, 128, ctypes.byref(nb), ctypes.byref(np_)) == P.PRISM_OK
+    assert (nb.value, np_.value) == (7 * 225, 7 * 225 * 128)
+    assert L.prism_zone_chunked_size(21, 68, 120, 3, 9, 16, 0, ctypes.byref(nb), ctypes.byref(np_)) == P.PRISM_EINVAL
+    shapes = (ctypes.c_int32 * 12)(1, 8, 16, 2, 8, 8, 4, 4, 8, 8, 4, 4)
+    z = ctypes.c_size_t(0)
+    assert L.prism_zone_perm_chunked(None, 21, 45, 80, 3, 9, 16, shapes, 4, 128, None, None, None, ctypes.byref(z),
+                                     None) == P.PRISM_OK
+    assert z.value >= 175 * 4
+    # the padded block order is whole blocks
+    p = ctypes.c_void_p(256)
+    assert L.prism_pool_score_chunked(p, p, p, P.PRISM_BF16, 1024, 1000, p, 1100, 8, 128, 128, None, None, None, 0,
+                                      p, p, None, None) == P.PRISM_EINVAL

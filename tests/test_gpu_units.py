@@ -321,18 +321,20 @@ def test_bounded_wait_times_out_and_context_survives():
     np.testing.assert_allclose(os_.cpu().numpy(), a.astype(np.float64) @ a.astype(np.float64).T, atol=1e-3)
 
 
-def test_bsa_bwd_split_kernels_match_oracle():
-    # The library's default backward is the fused kernel (dQ reduce-added in fp32); the
-    # split kernels (dQ recomputing S and dP per query block) are selected for a whole
-    # process by PRISM_BWD_SPLIT=1.  Run that process and compare it to the oracle too.
+def test_bsa_bwd_fused_kernel_matches_oracle():
+    # The library's default backward is the split pair of kernels (dQ recomputing S and
+    # dP per query block); the fused kernel (dQ reduce-added in fp32) is selected for a
+    # whole process by PRISM_BWD_FUSED=1.  Run that process and compare it to the oracle
+    # too, on random lists, dense lists and zone-chunked blocks.
     import os
     import subprocess
     import sys
 
     code = (
         "import sys; sys.path.insert(0, 'tests'); import test_gpu_units as t;"
-        "t.test_bsa_bwd_tensor_core_random_lists(2048, 3, 1); t.test_bsa_bwd_dense_matches_sdpa_autograd(); print('split ok')")
+        "t.test_bsa_bwd_tensor_core_random_lists(2048, 3, 1); t.test_bsa_bwd_dense_matches_sdpa_autograd();"
+        "import test_gpu_chunked as c; c.test_pool_and_attention_on_chunked_blocks('bf16', 128, 128); print('fused ok')")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, PRISM_BWD_SPLIT="1")
+    env = dict(os.environ, PRISM_BWD_FUSED="1")
     r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0 and "split ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+    assert r.returncode == 0 and "fused ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
