@@ -336,7 +336,7 @@ cudaError_t a2v_attn_launch(const void* qv, const void* ka, const void* va, int6
                             int M, int Hh, void* o, float* sqn, cudaStream_t st, uint32_t* status) {
   const int nbq = (N + kRows - 1) / kRows, nbk = (M + kRows - 1) / kRows;
   if (M > 32 * kMaxChunks)  // longer audio: the general kernel, every key block, online softmax
-    return attn_fwd_tc_launch(qv, ka, va, ld_v, ld_a, N, M, Hh, nullptr, nullptr, nbq, nbk, nullptr, o, nullptr, sqn,
+    return attn_fwd_tc_launch(qv, ka, va, ld_v, ld_a, N, M, Hh, nullptr, nullptr, nbq, nbk, nullptr, nullptr, o, nullptr, sqn,
                               "a2v_attn", st, status);
   CUtensorMap mq, mk, mv, mk1, mv1;
   const uint64_t inner = (uint64_t)Hh * kHd;

@@ -6,6 +6,12 @@
 //   (popcount + warp scan), so the result is deterministic.
 // row_dot: D[h][r] = sum_c dO[r, h, c] * O[r, h, c] (fp32), the softmax-gradient
 //   row term of dS = P * (dP - D).
+// order_rows: the launch order of the attention kernels' CTAs.  A CTA's work is its
+//   list length; under the CDF rule lengths differ by up to two orders of magnitude
+//   within a head, so a long row started late leaves the GPU idle at the end of the
+//   launch.  Within each head the rows are ordered by list length, longest first
+//   (equal lengths by index, so the order is deterministic); heads stay in sequence,
+//   which keeps the CTAs in flight on one or two heads' K and V (L2-resident).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -82,6 +88,50 @@ __global__ void row_dot_kernel(const T* __restrict__ o, const T* __restrict__ dO
   if (lane == 0) D[(size_t)h * N + n] = s;
 }
 
+
+// One warp per head: counting sort of the head's rows by list length, descending and
+// stable.  hist[0..nb] in dynamic shared memory.
+__global__ void __launch_bounds__(32) order_rows_kernel(const int32_t* __restrict__ counts, int nb,
+                                                        int32_t* __restrict__ order) {
+  extern __shared__ int32_t hist[];
+  const int h = blockIdx.x, lane = threadIdx.x;
+  const int32_t* c = counts + (size_t)h * nb;
+  auto key = [&](int i) { return min(max(c[i], 0), nb); };
+  for (int b = lane; b <= nb; b += 32) hist[b] = 0;
+  __syncwarp();
+  for (int i = lane; i < nb; i += 32) atomicAdd(&hist[key(i)], 1);
+  __syncwarp();
+  // hist[b] <- rows whose length exceeds b (their start in the order)
+  int run = 0;
+  for (int b0 = nb; b0 >= 0; b0 -= 32) {
+    const int b = b0 - lane;
+    const int v = b >= 0 ? hist[b] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (b >= 0) hist[b] = run + incl - v;
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int i0 = 0; i0 < nb; i0 += 32) {
+    const int i = i0 + lane;
+    const int k = i < nb ? key(i) : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, k);
+    const int rank = __popc(peers & lt);
+    const int base = i < nb ? hist[k] : 0;
+    __syncwarp();
+    if (i < nb) {
+      order[(size_t)h * nb + base + rank] = h * nb + i;
+      if (rank == 0) hist[k] = base + __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
 }  // namespace
 
 size_t lists_ws_bytes(int Hh, int nb) {
@@ -108,6 +158,16 @@ cudaError_t transpose_lists_launch(const int32_t* counts, const int32_t* idx, in
   const int64_t threads = (int64_t)Hh * nb * 32;
   HookScope hs("lists_emit", st);
   emit_lists_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(bits, Hh, nb, *tcounts, *tidx);
+  return cudaGetLastError();
+}
+
+bool order_rows_supported(int nb) { return nb >= 1 && (size_t)(nb + 1) * 4 <= kOrderSmemMax; }
+
+cudaError_t order_rows_launch(const int32_t* counts, int Hh, int nb, int32_t* order, const char* name,
+                              cudaStream_t st) {
+  if (!order_rows_supported(nb)) return cudaErrorInvalidValue;
+  HookScope hs(name, st);
+  order_rows_kernel<<<Hh, 32, (size_t)(nb + 1) * 4, st>>>(counts, nb, order);
   return cudaGetLastError();
 }
 

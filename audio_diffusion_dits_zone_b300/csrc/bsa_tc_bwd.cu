@@ -125,11 +125,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                      const float* __restrict__ L2, const float* __restrict__ Dp, int npad,
                      __nv_bfloat16* __restrict__ dq, int64_t ld, int N, const int32_t* __restrict__ counts,
-                     const int32_t* __restrict__ idx, int nb, const int32_t* __restrict__ blen, uint32_t* status) {
+                     const int32_t* __restrict__ idx, int nb, const int32_t* __restrict__ blen,
+                     const int32_t* __restrict__ order, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x;
+  const int item = order ? order[blockIdx.x] : (int)blockIdx.x;
+  if (item < 0 || item >= (int)gridDim.x) {
+    if (threadIdx.x == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
+    return;
+  }
   const int h = item / nb, i = item - h * nb;
   int cnt = counts[item];
   if (cnt < 0 || cnt > nb) cnt = cnt < 0 ? 0 : nb;
@@ -422,11 +427,15 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
                        const float* __restrict__ L2, const float* __restrict__ Dp, int npad,
                        __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int64_t ld, int N,
                        const int32_t* __restrict__ tcounts, const int32_t* __restrict__ tidx, int nb,
-                       const int32_t* __restrict__ blen, uint32_t* status) {
+                       const int32_t* __restrict__ blen, const int32_t* __restrict__ order, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   DkdvSmem& sm = *reinterpret_cast<DkdvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x;
+  const int item = order ? order[blockIdx.x] : (int)blockIdx.x;
+  if (item < 0 || item >= (int)gridDim.x) {
+    if (threadIdx.x == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
+    return;
+  }
   const int h = item / nb, j = item - h * nb;
   const int cnt = tcounts[item];
   const int32_t* lst = tidx + (size_t)item * nb;
@@ -737,7 +746,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                          const float* __restrict__ Dp, int npad, __nv_bfloat16* __restrict__ dk,
                          __nv_bfloat16* __restrict__ dv, int64_t ld, int N, const int32_t* __restrict__ tcounts,
                          const int32_t* __restrict__ tidx, int nb, const int32_t* __restrict__ blen,
-                         uint32_t* status) {
+                         const int32_t* __restrict__ order, uint32_t* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the swizzled tiles need it; never seen, but checked
     if (threadIdx.x == 0) flag_error(status, PRISM_DEV_TMEM);
@@ -745,7 +754,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
   FusedSmem& sm = *reinterpret_cast<FusedSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x;
+  const int item = order ? order[blockIdx.x] : (int)blockIdx.x;
+  if (item < 0 || item >= (int)gridDim.x) {
+    if (threadIdx.x == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
+    return;
+  }
   const int h = item / nb, j = item - h * nb;
   int cnt = tcounts[item];
   if (cnt < 0 || cnt > nb) cnt = cnt < 0 ? 0 : nb;
@@ -1100,8 +1113,9 @@ size_t bwd_tc_dqacc_bytes(int Hh, int nb) { return (size_t)nb * kB * Hh * kD * s
 cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,
                               const int32_t* idx, int nb, void* dq, void* dk, void* dv, const int32_t* tcounts,
-                              const int32_t* tidx, const int32_t* blen, float* rowstats, float* dqacc,
-                              cudaStream_t st, uint32_t* status) {
+                              const int32_t* tidx, const int32_t* blen, const int32_t* qorder,
+                              const int32_t* korder, float* rowstats, float* dqacc, cudaStream_t st,
+                              uint32_t* status) {
   const int npad = nb * kB;
   float* L2 = rowstats;
   float* Dp = rowstats + (size_t)Hh * npad;
@@ -1130,7 +1144,7 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
       HookScope hs("bsa_bwd_tc", st);
       bsa_bwd_fused_kernel<<<(unsigned)Hh * nb, kFusedThreads, kFusedSmemBytes, st>>>(
           mq, mk, mv, mdo, dqacc, L2, Dp, npad, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), ld,
-          N, tcounts, tidx, nb, blen, status);
+          N, tcounts, tidx, nb, blen, korder, status);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t vecs = (int64_t)N * Hh * (kD / 8);
@@ -1149,13 +1163,13 @@ cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const
   {
     HookScope hs("bsa_dq_tc", st);
     bsa_dq_tc_kernel<<<(unsigned)Hh * nb, kDqThreads, kDqSmemBytes, st>>>(
-        mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dq), ld, N, counts, idx, nb, blen, status);
+        mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dq), ld, N, counts, idx, nb, blen, qorder, status);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   HookScope hs("bsa_dkdv_tc", st);
   bsa_dkdv_tc_kernel<<<(unsigned)Hh * nb, kDkdvThreads, kDkdvSmemBytes, st>>>(
       mq, mk, mv, mdo, L2, Dp, npad, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), ld, N,
-      tcounts, tidx, nb, blen, status);
+      tcounts, tidx, nb, blen, korder, status);
   return cudaGetLastError();
 }
 

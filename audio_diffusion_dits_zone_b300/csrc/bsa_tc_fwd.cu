@@ -162,11 +162,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmv, __nv_bfloat16* __restrict__ o,
                       float* __restrict__ lse, float* __restrict__ sqn, int64_t ld, int N, int Nk,
                       const int32_t* __restrict__ counts, const int32_t* __restrict__ idx, int nbq,
-                      int nbk, const int32_t* __restrict__ blen, uint32_t* status) {
+                      int nbk, const int32_t* __restrict__ blen, const int32_t* __restrict__ order,
+                      uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x;  // head * nbq + query block
+  const int item = order ? order[blockIdx.x] : (int)blockIdx.x;  // head * nbq + query block
+  if (item < 0 || item >= (int)gridDim.x) {
+    if (threadIdx.x == 0) flag_error(status, PRISM_DEV_BAD_INDEX);
+    return;
+  }
   const int h = item / nbq, i = item - h * nbq;
   int cnt = counts ? counts[item] : nbk;  // no lists: every key block
   if (cnt < 0 || cnt > nbk) {
@@ -587,16 +592,16 @@ cudaError_t wait_timeout_selftest_launch(uint64_t limit_ns, int* marker, cudaStr
 }
 
 cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
-                              const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen, void* o,
-                              float* lse, cudaStream_t st, uint32_t* status) {
-  return attn_fwd_tc_launch(q, k, v, ld, ld, N, N, Hh, counts, idx, nb, nb, blen, o, lse, nullptr, "bsa_fwd_tc", st,
-                            status);
+                              const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen,
+                              const int32_t* order, void* o, float* lse, cudaStream_t st, uint32_t* status) {
+  return attn_fwd_tc_launch(q, k, v, ld, ld, N, N, Hh, counts, idx, nb, nb, blen, order, o, lse, nullptr, "bsa_fwd_tc",
+                            st, status);
 }
 
 cudaError_t attn_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int64_t ld_kv, int N,
                                int Nk, int Hh, const int32_t* counts, const int32_t* idx, int nbq, int nbk,
-                               const int32_t* blen, void* o, float* lse, float* sqn, const char* name,
-                               cudaStream_t st, uint32_t* status) {
+                               const int32_t* blen, const int32_t* order, void* o, float* lse, float* sqn,
+                               const char* name, cudaStream_t st, uint32_t* status) {
   CUtensorMap mq, mk, mv;
   const uint64_t inner = (uint64_t)Hh * kD;
   if (!tensor_map_2d_bf16(&mq, q, inner, N, (uint64_t)ld * 2, 64, kBM) ||
@@ -608,7 +613,7 @@ cudaError_t attn_fwd_tc_launch(const void* q, const void* k, const void* v, int6
   if (e != cudaSuccess) return e;
   HookScope hs(name, st);
   bsa_fwd_tc_kernel<<<(unsigned)Hh * nbq, kThreads, kFwdSmemBytes, st>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, sqn, ld, N, Nk, counts, idx, nbq, nbk, blen, status);
+      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, sqn, ld, N, Nk, counts, idx, nbq, nbk, blen, order, status);
   return cudaGetLastError();
 }
 

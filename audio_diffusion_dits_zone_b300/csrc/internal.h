@@ -87,6 +87,13 @@ cudaError_t bsa_bwd_simt_launch(const void* q, const void* k, const void* v, con
 
 // bsa_lists.cu (transposed kept lists and the backward row statistic)
 size_t lists_ws_bytes(int Hh, int nb);
+// Launch order of the attention kernels' CTAs: per head, rows by list length, longest
+// first (stable).  order [Hh * nb] receives h * nb + row.  Needs (nb + 1) * 4 bytes of
+// shared memory, at most kOrderSmemMax.
+constexpr size_t kOrderSmemMax = 48 * 1024;
+bool order_rows_supported(int nb);
+cudaError_t order_rows_launch(const int32_t* counts, int Hh, int nb, int32_t* order, const char* name,
+                              cudaStream_t st);
 cudaError_t transpose_lists_launch(const int32_t* counts, const int32_t* idx, int Hh, int nb, void* ws,
                                    int32_t** tcounts, int32_t** tidx, cudaStream_t st, uint32_t* status);
 cudaError_t row_dot_launch(const void* o, const void* dO, int dtype, int64_t ld, int N, int Hh, int d, float* Drow,
@@ -96,15 +103,17 @@ cudaError_t row_dot_launch(const void* o, const void* dO, int dtype, int64_t ld,
 // blen (nullable): tokens of each block (zone-chunked blocks); NULL = B-token chunks, the
 // last one short.
 cudaError_t bsa_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int N, int Hh,
-                              const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen, void* o,
-                              float* lse, cudaStream_t st, uint32_t* status);
+                              const int32_t* counts, const int32_t* idx, int nb, const int32_t* blen,
+                              const int32_t* order, void* o, float* lse, cudaStream_t st, uint32_t* status);
 // The same kernel with a key sequence of its own (Nk tokens in nbk blocks, row stride
 // ld_kv) and optional outputs: o, lse and sqn ([Hh][N] fp32, the squared L2 norm of each
 // normalised output row) may each be NULL.  counts == NULL visits every key block.
+// order (nullable, from order_rows_launch): CTA b processes item order[b]; NULL = item b.
+// The items are independent, so the order changes the schedule, not the results.
 cudaError_t attn_fwd_tc_launch(const void* q, const void* k, const void* v, int64_t ld, int64_t ld_kv, int N,
                                int Nk, int Hh, const int32_t* counts, const int32_t* idx, int nbq, int nbk,
-                               const int32_t* blen, void* o, float* lse, float* sqn, const char* name,
-                               cudaStream_t st, uint32_t* status);
+                               const int32_t* blen, const int32_t* order, void* o, float* lse, float* sqn,
+                               const char* name, cudaStream_t st, uint32_t* status);
 // The cross-attention of the A2V field (a2v.cu): sqn[h][n] = |O[n][h]|^2, O optional.
 cudaError_t a2v_attn_launch(const void* qv, const void* ka, const void* va, int64_t ld_v, int64_t ld_a, int N,
                             int M, int Hh, void* o, float* sqn, cudaStream_t st, uint32_t* status);
@@ -115,12 +124,14 @@ size_t bwd_tc_rowstats_bytes(int Hh, int nb);
 size_t bwd_tc_dqacc_bytes(int Hh, int nb);
 // dqacc != NULL: the fused kernel (dK, dV and dQ in one pass over the transposed lists,
 // dQ reduce-added into dqacc, then converted); dqacc == NULL: the split kernels (dQ per
-// query block, recomputing S and dP; dK and dV per key block).
+// query block, recomputing S and dP; dK and dV per key block).  qorder / korder
+// (nullable): launch orders of the query-block (dQ) and key-block (dK/dV, fused) CTAs.
 cudaError_t bsa_bwd_tc_launch(const void* q, const void* k, const void* v, const void* o, const void* dO,
                               const float* lse, int64_t ld, int N, int Hh, const int32_t* counts,
                               const int32_t* idx, int nb, void* dq, void* dk, void* dv, const int32_t* tcounts,
-                              const int32_t* tidx, const int32_t* blen, float* rowstats, float* dqacc,
-                              cudaStream_t st, uint32_t* status);
+                              const int32_t* tidx, const int32_t* blen, const int32_t* qorder,
+                              const int32_t* korder, float* rowstats, float* dqacc, cudaStream_t st,
+                              uint32_t* status);
 
 // pab.cu: per-head mean squared difference of two [N][Hh][d] tensors (row stride ld);
 // part holds Hh * attn_mse_chunks(N, Hh) fp32 partial sums.

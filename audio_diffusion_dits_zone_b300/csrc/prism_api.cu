@@ -354,17 +354,24 @@ int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32
                   const int32_t* blen, void* o_blk, float* lse, void* ws, size_t* ws_bytes, void* stream) {
   int rc = check_attention_args(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb);
   if (rc != PRISM_OK) return rc;
-  if (ws_query(ws, ws_bytes, ws_round(0), &rc)) return rc;
+  // workspace (tensor-core path): the CTAs' launch order, longest lists first per head
+  const bool tc = use_tc(dtype, d, B, ld, {q_blk, k_blk, v_blk, o_blk});
+  const bool ordered = tc && prism::order_rows_supported(nb);
+  if (ws_query(ws, ws_bytes, ws_round(ordered ? (size_t)Hh * nb * sizeof(int32_t) : 0), &rc)) return rc;
   if (!o_blk || !lse) return fail(PRISM_EINVAL, "NULL output pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (use_tc(dtype, d, B, ld, {q_blk, k_blk, v_blk, o_blk}))
-    e = prism::bsa_fwd_tc_launch(q_blk, k_blk, v_blk, ld, N, Hh, counts, idx, nb, blen, o_blk, lse, st,
-                                 status_ptr());
-  else
-    e = prism::bsa_fwd_simt_launch(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb, blen, o_blk, lse, st,
+  cudaError_t e = cudaSuccess;
+  int32_t* order = ordered ? static_cast<int32_t*>(ws) : nullptr;
+  if (ordered) e = prism::order_rows_launch(counts, Hh, nb, order, "order_rows", st);
+  if (e == cudaSuccess) {
+    if (tc)
+      e = prism::bsa_fwd_tc_launch(q_blk, k_blk, v_blk, ld, N, Hh, counts, idx, nb, blen, order, o_blk, lse, st,
                                    status_ptr());
-  return e == cudaSuccess ? (launched(1), ok()) : cuda_fail(e, "prism_bsa_fwd");
+    else
+      e = prism::bsa_fwd_simt_launch(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb, blen, o_blk, lse,
+                                     st, status_ptr());
+  }
+  return e == cudaSuccess ? (launched(ordered ? 2 : 1), ok()) : cuda_fail(e, "prism_bsa_fwd");
 }
 
 int prism_a2v_norm(const void* qv, const void* ka, const void* va, int32_t dtype, int64_t ld_v, int64_t ld_a,
@@ -393,30 +400,38 @@ int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk, const
                   void* dv, void* ws, size_t* ws_bytes, void* stream) {
   int rc = check_attention_args(q_blk, k_blk, v_blk, dtype, ld, N, Hh, d, B, counts, idx, nb);
   if (rc != PRISM_OK) return rc;
-  // workspace: transposed lists | row statistics | (fused tensor-core path) fp32 dQ accumulator
+  // workspace: transposed lists | row statistics | (tensor-core path) launch orders of
+  // the query-block and key-block CTAs | (fused tensor-core path) fp32 dQ accumulator
   auto r256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t lists = r256(prism::lists_ws_bytes(Hh, nb));
   const bool tc = use_tc(dtype, d, B, ld, {q_blk, k_blk, v_blk, o_blk, do_blk, dq, dk, dv});
   const bool fused = tc && fused_backward();
+  const bool ordered = tc && prism::order_rows_supported(nb);
   const size_t rows = r256(tc ? prism::bwd_tc_rowstats_bytes(Hh, nb) : (size_t)Hh * N * sizeof(float));
+  const size_t ord = ordered ? 2 * r256((size_t)Hh * nb * sizeof(int32_t)) : 0;
   const size_t acc = fused ? prism::bwd_tc_dqacc_bytes(Hh, nb) : 0;
-  if (ws_query(ws, ws_bytes, ws_round(lists + rows + acc), &rc)) return rc;
+  if (ws_query(ws, ws_bytes, ws_round(lists + rows + ord + acc), &rc)) return rc;
   if (!o_blk || !do_blk || !lse || !dq || !dk || !dv) return fail(PRISM_EINVAL, "NULL pointer");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* tcounts = nullptr;
   int32_t* tidx = nullptr;
   float* rowstats = reinterpret_cast<float*>(static_cast<char*>(ws) + lists);
-  float* dqacc = fused ? reinterpret_cast<float*>(static_cast<char*>(ws) + lists + rows) : nullptr;
+  int32_t* qorder = ordered ? reinterpret_cast<int32_t*>(static_cast<char*>(ws) + lists + rows) : nullptr;
+  int32_t* korder = ordered ? qorder + ord / (2 * sizeof(int32_t)) : nullptr;
+  float* dqacc = fused ? reinterpret_cast<float*>(static_cast<char*>(ws) + lists + rows + ord) : nullptr;
   cudaError_t e = prism::transpose_lists_launch(counts, idx, Hh, nb, ws, &tcounts, &tidx, st, status_ptr());
+  if (e == cudaSuccess && ordered && !fused) e = prism::order_rows_launch(counts, Hh, nb, qorder, "order_rows_q", st);
+  if (e == cudaSuccess && ordered) e = prism::order_rows_launch(tcounts, Hh, nb, korder, "order_rows_k", st);
   if (e == cudaSuccess) {
     if (tc)
       e = prism::bsa_bwd_tc_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, ld, N, Hh, counts, idx, nb, dq, dk, dv,
-                                   tcounts, tidx, blen, rowstats, dqacc, st, status_ptr());
+                                   tcounts, tidx, blen, fused ? nullptr : qorder, korder, rowstats, dqacc, st,
+                                   status_ptr());
     else
       e = prism::bsa_bwd_simt_launch(q_blk, k_blk, v_blk, o_blk, do_blk, lse, dtype, ld, N, Hh, d, B, counts, idx,
                                      nb, blen, dq, dk, dv, tcounts, tidx, rowstats, st, status_ptr());
   }
-  return e == cudaSuccess ? (launched(5), ok()) : cuda_fail(e, "prism_bsa_bwd");
+  return e == cudaSuccess ? (launched(5 + (ordered ? (fused ? 1 : 2) : 0)), ok()) : cuda_fail(e, "prism_bsa_bwd");
 }
 
 int prism_attn_mse(const void* a, const void* b, int32_t dtype, int64_t ld, int32_t N, int32_t Hh, int32_t d,

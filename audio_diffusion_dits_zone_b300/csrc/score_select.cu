@@ -234,26 +234,33 @@ __device__ int select_row(const float* sv, int nb, int k_top, double tau, uint8_
       done = true;
     } else if (L <= (uint32_t)kCandCap) {
       // rank r of a candidate = candidates before it in (score desc, index asc) order;
-      // keep the first `best` for the smallest best that completes both conditions
+      // keep the first `best` for the smallest best that completes both conditions.
+      // The histogram is spent: it holds the candidates' order keys and masses, computed
+      // once; candidates are in index order, so "index before" is "position before".
+      uint32_t* ckey = cnt;
+      unsigned long long* cmass = mass;
+      for (uint32_t c = lane; c < L; c += 32) {
+        const float v = sv[cand[c]];
+        ckey[c] = order_bits(v);
+        cmass[c] = mass_of(v, mx);
+      }
+      __syncwarp();
       uint32_t best = L;
       for (uint32_t c0 = 0; c0 < L; c0 += 32) {
         const uint32_t c = c0 + lane;
         uint32_t take = 0xffffffffu;
         if (c < L) {
-          const int ti = cand[c];
-          const uint32_t key = order_bits(sv[ti]);
+          const uint32_t key = ckey[c];
           uint32_t rank = 0u;
           unsigned long long pre = 0ull;
           for (uint32_t dd = 0; dd < L; ++dd) {
-            const int td = cand[dd];
-            const float vd = sv[td];
-            const uint32_t kd = order_bits(vd);
-            if (kd > key || (kd == key && td < ti)) {
+            const uint32_t kd = ckey[dd];
+            if (kd > key || (kd == key && dd < c)) {
               ++rank;
-              pre += mass_of(vd, mx);
+              pre += cmass[dd];
             }
           }
-          if (above + rank + 1u >= kneed && above_m + pre + mass_of(sv[ti], mx) >= target) take = rank + 1u;
+          if (above + rank + 1u >= kneed && above_m + pre + cmass[c] >= target) take = rank + 1u;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) take = min(take, __shfl_xor_sync(0xffffffffu, take, o));
@@ -265,12 +272,11 @@ __device__ int select_row(const float* sv, int nb, int k_top, double tau, uint8_
         int ti = 0;
         if (c < L) {
           ti = cand[c];
-          const uint32_t key = order_bits(sv[ti]);
+          const uint32_t key = ckey[c];
           uint32_t rank = 0u;
           for (uint32_t dd = 0; dd < L; ++dd) {
-            const int td = cand[dd];
-            const uint32_t kd = order_bits(sv[td]);
-            rank += (kd > key || (kd == key && td < ti)) ? 1u : 0u;
+            const uint32_t kd = ckey[dd];
+            rank += (kd > key || (kd == key && dd < c)) ? 1u : 0u;
           }
           k = rank < best;
         }

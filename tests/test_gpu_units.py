@@ -303,6 +303,55 @@ def test_bsa_bwd_tensor_core_random_lists(N, heads, seed):
     attn_close(dv.float().cpu().numpy(), dV, what="dV")
 
 
+def skewed_lists(nb, heads, seed):
+    """Lists whose lengths span 0..nb with many equal lengths, ordered differently in
+    each head (falling, rising, shuffled): the attention kernels launch their CTAs
+    longest list first within each head, so these exercise that order."""
+    rng = np.random.default_rng(seed)
+    base = np.minimum(nb, np.maximum(0, np.round(nb * rng.pareto(1.5, nb) / 6).astype(np.int32)))
+    base[:3] = (nb, 0, 1)
+    counts = np.empty((heads, nb), np.int32)
+    for h in range(heads):
+        c = np.sort(base)[::-1] if h % 3 == 0 else (np.sort(base) if h % 3 == 1 else rng.permutation(base))
+        counts[h] = c
+    idx = np.full((heads, nb, nb), -1, np.int32)
+    for h in range(heads):
+        for i in range(nb):
+            idx[h, i, :counts[h, i]] = np.sort(rng.choice(nb, counts[h, i], replace=False))
+    return counts, idx
+
+
+def test_attention_with_skewed_list_lengths():
+    # forward and backward on lists of very unequal lengths (the CTAs run longest first)
+    wl = small_workload((1, 1, 40 * 128 - 37), 3, 128, "bf16", 128)
+    Q, K, V = qkv(wl)
+    dO = np.stack(synth.gen_heads(wl, synth.DO_ID, range(3)), axis=1)
+    nb, N, B = wl.nb, wl.N, 128
+    counts, idx = skewed_lists(nb, 3, seed=11)
+    assert len(set(counts[0].tolist())) < nb  # equal lengths present
+    f64 = lambda x: x.astype(np.float64)  # noqa: E731
+    oO, oL = po.bsa_forward(f64(Q), f64(K), f64(V), counts, idx, B)
+    q, k, v, g = (to_dev(x, torch.bfloat16) for x in (Q, K, V, dO))
+    tc, ti = torch.from_numpy(counts).to(dev), torch.from_numpy(idx).to(dev)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((3, N), float("nan"), device=dev)
+    P.prism_bsa_fwd(q, k, v, B, tc, ti, o, lse)
+    assert P.status_check() == 0
+    attn_close(o.float().cpu().numpy(), oO, what="O", max_abs=2e-2, mean_abs=2e-3)
+    fin = np.isfinite(oL)
+    L = lse.cpu().numpy()
+    assert np.array_equal(np.isfinite(L), fin)
+    np.testing.assert_allclose(L[fin], oL[fin], atol=2e-3)
+    O_in = synth.round_inputs(wl, oO.astype(np.float32))
+    L_in = oL.astype(np.float32)
+    dQ, dK, dV = po.bsa_backward(f64(Q), f64(K), f64(V), f64(O_in), f64(dO), f64(L_in), counts, idx, B)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    P.prism_bsa_bwd(q, k, v, to_dev(O_in, torch.bfloat16), g, torch.from_numpy(L_in).to(dev), B, tc, ti, dq, dk, dv)
+    assert P.status_check() == 0
+    for got, ref, what in ((dq, dQ, "dQ"), (dk, dK, "dK"), (dv, dV, "dV")):
+        attn_close(got.float().cpu().numpy(), ref, what=what, max_abs=2e-2, mean_abs=2e-3)
+
+
 def test_bounded_wait_times_out_and_context_survives():
     # A wait that nothing satisfies gives up after 5 ms, flags the status word and the
     # kernel exits normally; the next call on the same context still works.
