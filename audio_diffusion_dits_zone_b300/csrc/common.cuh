@@ -362,11 +362,6 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 
 // Shared-memory writes of this thread become visible to the async proxy (tensor-core
 // operand reads, bulk copies) once the thread has executed this fence.
-// Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads (a multiple of 32):
-// every participating warp arrives with all its threads.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -334,10 +334,12 @@ __device__ __forceinline__ void zone_slab_sums(const uint8_t* slab, int lane, f2
 // part[(z * nchunks + chunk) * 3 + a] exactly as zone_lines_kernel (chunk = 64 channels),
 // from slabs loaded with the 4D tensor map tm = feature viewed as [T][H][W][C] bf16 with
 // box {64, kWq, MH, MT}.  Persistent CTAs of kTmaWarps warps; each warp streams its own
-// items, nq slabs (kWq columns each) per item, through a kTmaStages-stage ring that its
-// lane 0 refills (so the next slabs are in flight while this one is reduced).  Zones that fill the box
-// take the unpredicated path; zones clipped by the grid (or smaller than the box) mask
-// the positions outside them, whose slab bytes are zero fill or a neighbour's tokens.
+// items, up to nq slabs (kWq columns each) per item, through a kTmaStages-stage ring
+// that its lane 0 refills (so the next slabs are in flight while this one is reduced).
+// A zone cut short in w by the grid has only ceil(Lw / kWq) slabs (the ones wholly
+// outside it are never loaded).  Slabs that lie inside the zone take the unpredicated
+// path; the others (zones clipped in t or h, a last slab partly outside) mask the
+// positions outside the zone, whose slab bytes are zero fill or a neighbour's tokens.
 template <int MT, int MH>
 __global__ void __launch_bounds__(kTmaWarps * 32, 1)
     zone_tma_kernel(const __grid_constant__ CUtensorMap tm, ZoneGeom g, int nchunks, int items, int nq,
@@ -355,26 +357,46 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1)
   const int stride = gridDim.x * kTmaWarps;
   const int first = blockIdx.x * kTmaWarps + warp;
   const int nmine = first < items ? (items - first + stride - 1) / stride : 0;
-  const int nslabs = nq * nmine;
-  auto issue = [&](int s) {  // slab s of this warp -> stage s % kTmaStages
-    const int n = s / nq, q = s - n * nq;
-    const int k = first + n * stride;
+  // the slabs of item n: the zone's w extent in kWq-column steps
+  auto nq_of = [&](int n) {
+    const ZoneBox b = zone_box(g, (first + n * stride) / nchunks);
+    return min(nq, (b.Lw + kWq - 1) / kWq);
+  };
+  // a position in this warp's slab sequence: item n, slab q of its nqn
+  struct Cursor {
+    int n, q, nqn;
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.q == c.nqn) {
+      ++c.n;
+      c.q = 0;
+      c.nqn = c.n < nmine ? nq_of(c.n) : 0;
+    }
+  };
+  auto issue = [&](const Cursor& c, int s) {  // the warp's slab number s -> stage s % kTmaStages
+    const int k = first + c.n * stride;
     const int z = k / nchunks, chunk = k - z * nchunks;
     const ZoneBox b = zone_box(g, z);
     const uint32_t bar = smem_u32(&sm.full[warp][s % kTmaStages]);
     mbar_arrive_expect_tx(bar, (uint32_t)(MT * MH * kWq * kSlabCh * 2));
-    tma_load_4d(smem_u32(sm.slab[warp][s % kTmaStages]), &tm, chunk * kSlabCh, b.w0 + q * kWq, b.h0, b.t0, bar);
+    tma_load_4d(smem_u32(sm.slab[warp][s % kTmaStages]), &tm, chunk * kSlabCh, b.w0 + c.q * kWq, b.h0, b.t0, bar);
   };
-  int issued = 0;  // lane 0: slabs issued so far
+  Cursor pc{0, 0, nmine > 0 ? nq_of(0) : 0};  // lane 0: the next slab to load
+  int issued = 0;                              // lane 0: slabs issued so far
   if (lane == 0) {
     tma_prefetch_desc(&tm);
-    for (int s = 0; s < kTmaStages && s < nslabs; ++s) issue(s), ++issued;
+    while (issued < kTmaStages && pc.n < nmine) {
+      issue(pc, issued);
+      ++issued;
+      advance(pc);
+    }
   }
   int abort = 0;
   const f2 zero{0ull};
   f2 wsum[MT][MH], sq[MT], bt = zero, bh = zero, nx0 = zero;
-  for (int s = 0; s < nslabs; ++s) {
-    const int n = s / nq, q = s - n * nq;
+  Cursor cc{0, 0, nmine > 0 ? nq_of(0) : 0};  // the slab to reduce
+  for (int s = 0; cc.n < nmine; ++s) {
+    const int n = cc.n, q = cc.q;
     const int k = first + n * stride;
     const int z = k / nchunks, chunk = k - z * nchunks;
     const ZoneBox b = zone_box(g, z);
@@ -398,10 +420,14 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1)
       zone_slab_sums<MT, MH, false>(slab, lane, nx0, MT, MH, kWq, wsum, sq, bt, bh);
     else
       zone_slab_sums<MT, MH, true>(slab, lane, nx0, b.Lt, b.Lh, wlim, wsum, sq, bt, bh);
-    // every lane has read the stage: refill it with slab s + 2
+    // every lane has read the stage: refill it with slab s + kTmaStages
     __syncwarp();
-    if (lane == 0 && s + kTmaStages < nslabs) issue(s + kTmaStages), ++issued;
-    if (q == nq - 1) {  // the item's last slab: one partial per (zone, 64 channels)
+    if (lane == 0 && pc.n < nmine) {
+      issue(pc, issued);
+      ++issued;
+      advance(pc);
+    }
+    if (q == cc.nqn - 1) {  // the item's last slab: one partial per (zone, 64 channels)
       f2 bw = zero;
 #pragma unroll
       for (int t = 0; t < MT; ++t)
@@ -429,6 +455,7 @@ __global__ void __launch_bounds__(kTmaWarps * 32, 1)
         for (int o = 16; o > 0; o >>= 1) ss[a] += __shfl_xor_sync(0xffffffffu, ss[a], o);
       if (lane < 3) part[((size_t)z * nchunks + chunk) * 3 + lane] = lane == 0 ? ss[0] : (lane == 1 ? ss[1] : ss[2]);
     }
+    advance(cc);
   }
   // a warp that gave up waits (bounded) for the copies it still has in flight: the
   // last slab issued into each stage completes that stage's phase (slab / stages) & 1

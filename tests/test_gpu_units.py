@@ -53,7 +53,10 @@ def test_umma_layout_selftest():
 # ----------------------------------------------------------------------- zone
 @pytest.mark.parametrize("grid,zext,heads,d,dtype", [((5, 8, 16), (5, 4, 8), 2, 64, "f32"),
                                                      ((7, 20, 40), (3, 9, 16), 3, 128, "bf16"),
-                                                     ((6, 16, 32), (3, 8, 16), 1, 128, "bf16")])
+                                                     ((6, 16, 32), (3, 8, 16), 1, 128, "bf16"),
+                                                     # last zones 1 x 2 x 6: a short w extent whose
+                                                     # second slab is partly outside the zone
+                                                     ((4, 11, 38), (3, 9, 16), 2, 128, "bf16")])
 def test_zone_shapes_match_oracle(grid, zext, heads, d, dtype):
     wl = small_workload(grid, heads, d, dtype, 128 if d == 128 else 64)
     V = np.stack(synth.gen_heads(wl, synth.V_ID, range(heads)), axis=1)  # [N, Hh, d]
