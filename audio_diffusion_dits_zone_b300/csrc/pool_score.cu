@@ -142,10 +142,12 @@ __global__ void __launch_bounds__(kPoolThreads)
 }
 
 // scores: S = qbar kbar^T / sqrt(d) per head, fp32 on CUDA cores.  A CTA of 256
-// threads owns a 128 x 128 tile of S; each thread an 8 x 8 register tile (rows
-// ty + 16u, columns tx + 16w).  k-slices of 16 are staged in shared memory,
-// transposed (k-major), double-buffered through registers so the next slice's
-// global loads overlap this slice's 8 x 8 x 16 FMAs.
+// threads owns a 128 x 128 tile of S; each thread an 8 x 8 register tile: rows
+// 4ty .. 4ty + 3 and 64 + 4ty .. 64 + 4ty + 3, columns likewise from 4tx, so each
+// channel step is four 16-byte shared loads for 64 FMAs.  k-slices of 16 are staged
+// in shared memory, transposed (k-major), double-buffered through registers so the
+// next slice's global loads overlap this slice's 8 x 8 x 16 FMAs.  Every score is one
+// FMA chain over the channels in ascending order, then the scale.
 constexpr int kSTile = 128, kSK = 16, kSThreads = 256;
 
 __global__ void __launch_bounds__(kSThreads) scores_kernel(const float* __restrict__ qbar,
@@ -219,12 +221,12 @@ __global__ void __launch_bounds__(kSThreads) scores_kernel(const float* __restri
     if (kt + 1 < nk) load((kt + 1) * kSK);
 #pragma unroll
     for (int c = 0; c < kSK; ++c) {
-      float a[8], b[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        a[u] = As[buf][c][ty + 16 * u];
-        b[u] = Bs[buf][c][tx + 16 * u];
-      }
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][c][4 * ty]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][c][64 + 4 * ty]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][c][4 * tx]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][c][64 + 4 * tx]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
       for (int u = 0; u < 8; ++u)
 #pragma unroll
@@ -235,12 +237,12 @@ __global__ void __launch_bounds__(kSThreads) scores_kernel(const float* __restri
   }
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    const int i = i0 + ty + 16 * u;
+    const int i = i0 + (u & 3) + 4 * ty + 64 * (u >> 2);
     if (i >= nb) continue;
     float* row = S + ((size_t)h * nb + i) * nb;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      const int j = j0 + tx + 16 * w;
+      const int j = j0 + (w & 3) + 4 * tx + 64 * (w >> 2);
       if (j < nb) row[j] = acc[u][w] * scale;
     }
   }
