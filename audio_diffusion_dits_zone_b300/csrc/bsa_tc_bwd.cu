@@ -12,8 +12,8 @@
 //             rows get P = 0) and D[h][r], padded to whole blocks so the attention
 //             kernels can bulk-copy 128 of them at a time;
 //   dq        one CTA per (head, query block) walking its kept list:
-//               S_b = Q K_j^T (TMEM, double-buffered), dP = dO V_j^T (TMEM),
-//               dS = P (dP - D) in bf16 into the S buffer, dQ += dS K_j (A from TMEM);
+//               S = Q K_j^T (TMEM), dP = dO V_j^T (TMEM), dS = P (dP - D) in bf16 into
+//               a TMEM buffer of its own (double-buffered), dQ += dS K_j (A from TMEM);
 //   dkdv      one CTA per (head, key block) walking the query blocks that kept it:
 //               S^T = K_j Q_i^T, dP^T = V_j dO_i^T (TMEM),
 //               P^T, dS^T in bf16 into those buffers, dV += P^T dO_i, dK += dS^T Q_i.
@@ -100,9 +100,9 @@ struct DqSmem {
   uint64_t q_full;
   uint64_t k_full[kDqKStages], k_empty[kDqKStages];  // K_t: read by S(t) and dQ(t)
   uint64_t v_full[kDqVStages], v_empty[kDqVStages];  // V_t: read by dP(t) only
-  uint64_t s_full[2], dp_full, dp_free;
-  uint64_t ds_full[2][2];  // [S buffer][key half]
-  uint64_t dq_done[2];     // dQ(t) has read S buffer t & 1
+  uint64_t s_full, dp_full, dp_free;  // dp_free: S(t) and dP(t) are in the softmax's registers
+  uint64_t ds_full[2][2];  // [dS buffer][key half]
+  uint64_t dq_done[2];     // dQ(t) has read dS buffer t & 1
   uint64_t a_issued;       // the S / dP issuer has enqueued block t + 1's products
   uint64_t acc_done, in_done;
   uint32_t tmem_base;
@@ -111,15 +111,15 @@ struct DqSmem {
 constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024;
 static_assert(kDqSmemBytes <= 232448, "shared memory budget");
 
-// TMEM: S0 [0,128) S1 [128,256) dP [256,384) dQ [384,512).
+// TMEM: S [0,128) dS0 [128,192) dS1 [192,256) dP [256,384) dQ [384,512).
 // Two issuing threads:
-//   warp 1   dP(t+1) as soon as both halves have loaded dP(t) (dP is single-buffered),
-//            then S(t+1) into S buffer (t+1) & 1 once dQ(t-1), its last reader, has
-//            completed; so the next block's inputs are computed while block t's
-//            gradient is formed;
+//   warp 1   dP(t+1) and S(t+1) as soon as both halves have loaded S(t) and dP(t) into
+//            registers (S and dP are single-buffered), so the next block's inputs are
+//            computed while block t's gradient is formed, whatever the dQ products do;
 //   warp 10  dQ(t) += dS(t) K_t in two K = 64 steps, one per key half, as soon as that
 //            half's warpgroup has written it;
-// dS (bf16) overwrites the S half it came from.
+// dS(t) (bf16 pairs) goes into dS buffer t & 1, which the softmax overwrites only after
+// dQ(t - 2), its last reader, has completed.
 __global__ void __launch_bounds__(kDqThreads, 1)
     bsa_dq_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       mbar_init(smem_u32(&sm.v_full[s]), 1);
       mbar_init(smem_u32(&sm.v_empty[s]), 1);
     }
+    mbar_init(smem_u32(&sm.s_full), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&sm.s_full[s]), 1);
       mbar_init(smem_u32(&sm.ds_full[s][0]), 4);
       mbar_init(smem_u32(&sm.ds_full[s][1]), 4);
     }
@@ -227,12 +227,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tc_commit(smem_u32(&sm.dp_full));
         tc_commit(smem_u32(&sm.v_empty[vs]));
       };
-      auto issue_s = [&](int t) {  // S(t) = Q K_t^T into S buffer t & 1
+      auto issue_s = [&](int t) {  // S(t) = Q K_t^T
         const uint64_t dk = desc_at(dk0, (t % kDqKStages) * kTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + (t & 1) * 128, desc_at(dq_q, koff(kk)), desc_at(dk, koff(kk)), id_ss, kk > 0);
-        tc_commit(smem_u32(&sm.s_full[t & 1]));
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tmem, desc_at(dq_q, koff(kk)), desc_at(dk, koff(kk)), id_ss, kk > 0);
+        tc_commit(smem_u32(&sm.s_full));
       };
       bool ok = mbar_wait(smem_u32(&sm.q_full), 0, abort, status) &&
                 mbar_wait(smem_u32(&sm.v_full[0]), 0, abort, status) &&
@@ -249,7 +248,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tc_fence_after();
         issue_dp(t);
         if (!(ok = mbar_wait(smem_u32(&sm.k_full[t % kDqKStages]), (t / kDqKStages) & 1, abort, status))) break;
-        if (it >= 1 && !(ok = mbar_wait(smem_u32(&sm.dq_done[t & 1]), ((it - 1) >> 1) & 1, abort, status))) break;
         tc_fence_after();
         issue_s(t);
         mbar_arrive(smem_u32(&sm.a_issued));  // dQ(t - 1) may follow them into the tensor pipe
@@ -274,7 +272,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + 384, tmem + b * 128 + half * 64 + kk * 8, desc_at(dkt, (half * 4 + kk) * 2048), id_ts,
+            mma_ts(tmem + 384, tmem + 128 + b * 64 + half * 32 + kk * 8, desc_at(dkt, (half * 4 + kk) * 2048), id_ts,
                    (it > 0 || half > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
@@ -302,14 +300,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const int b = it & 1;
       const int j = j_next;
       if (it + 1 < cnt) j_next = lst[it + 1];
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[b]), (it >> 1) & 1, abort, status) &&
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full), it & 1, abort, status) &&
                                        mbar_wait(smem_u32(&sm.dp_full), it & 1, abort, status));
       if (!ok) break;
       tc_fence_after();
       const int len = (j >= 0 && j < nb) ? (blen ? min(kB, max(0, blen[j])) : min(kB, N - j * kB)) : 0;
       uint32_t s0[32], s1[32], d0[32], d1[32];
-      tmem_ld32(lane_base + b * 128 + c0, s0);
-      tmem_ld32(lane_base + b * 128 + c0 + 32, s1);
+      tmem_ld32(lane_base + c0, s0);
+      tmem_ld32(lane_base + c0 + 32, s1);
       tmem_ld32(lane_base + 256 + c0, d0);
       tmem_ld32(lane_base + 256 + c0 + 32, d1);
       tmem_wait_ld();
@@ -317,7 +315,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       reg_fence(s1);
       reg_fence(d0);
       reg_fence(d1);
-      // dP is in registers: the next block's dO V^T may overwrite it
+      // S and dP are in registers: the next block's products may overwrite them
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.dp_free));
@@ -327,6 +325,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           if (c0 + x >= len) s0[x] = __float_as_uint(-INFINITY);
           if (c0 + 32 + x >= len) s1[x] = __float_as_uint(-INFINITY);
         }
+      }
+      // dS buffer b was last read by dQ(it - 2): long done unless the tensor pipe is far
+      // behind (a completed phase is seen by the non-blocking test at once)
+      if (it >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_done[b]), ((it >> 1) - 1) & 1, abort, status));
+        if (!ok) break;
+        tc_fence_after();
       }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           const f2 g = f2_add(f2_make(__uint_as_float(pr[2 * x]), __uint_as_float(pr[2 * x + 1])), neg_dr);
           pk[x] = f2_pack_bf16(f2_mul(p, g));  // dS = P (dP - D)
         }
-        tmem_st16(lane_base + b * 128 + c0 + cc * 16, pk);
+        tmem_st16(lane_base + 128 + b * 64 + half * 32 + cc * 16, pk);
       }
       tmem_wait_st();
       tc_fence_before();
