@@ -348,8 +348,8 @@ def run_e2e(layer, args, world):
     h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs(layer)] for _ in range(2)]
     s_in, s_run, s_out = (torch.cuda.Stream(layer.device) for _ in range(3))
     # the first step's inputs and the last step's outputs cannot overlap compute: time
-    # enough steps for the steady state to dominate
-    steps = max(12, min(args.steps, 20))
+    # enough steps (about two seconds of work) for the steady state to dominate
+    steps = max(20, min(args.steps, 40))
 
     def run(n):
         ran, out = [None, None], [None, None]
