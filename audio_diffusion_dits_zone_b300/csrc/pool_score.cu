@@ -146,11 +146,12 @@ __global__ void __launch_bounds__(kPoolThreads)
 // 4ty .. 4ty + 3 and 64 + 4ty .. 64 + 4ty + 3, columns likewise from 4tx, so each
 // channel step is four 16-byte shared loads for 64 FMAs.  k-slices of 16 are staged
 // in shared memory, transposed (k-major), double-buffered through registers so the
-// next slice's global loads overlap this slice's 8 x 8 x 16 FMAs.  Every score is one
-// FMA chain over the channels in ascending order, then the scale.
+// next slice's global loads overlap this slice's 8 x 8 x 16 FMAs, issued as packed
+// pairs (fma.rn.f32x2: two independent round-to-nearest FMAs per instruction).  Every
+// score is one FMA chain over the channels in ascending order, then the scale.
 constexpr int kSTile = 128, kSK = 16, kSThreads = 256;
 
-__global__ void __launch_bounds__(kSThreads) scores_kernel(const float* __restrict__ qbar,
+__global__ void __launch_bounds__(kSThreads, 2) scores_kernel(const float* __restrict__ qbar,
                                                            const float* __restrict__ kbar, int nb, int d,
                                                            float scale, float* __restrict__ S) {
   __shared__ __align__(16) float As[2][kSK][kSTile + 4];
@@ -207,11 +208,11 @@ __global__ void __launch_bounds__(kSThreads) scores_kernel(const float* __restri
       Bs[buf][lc + 3][r] = rb[u].w;
     }
   };
-  float acc[8][8];
+  f2 acc[8][4];  // columns (2w2, 2w2 + 1) of the 8 x 8 tile
 #pragma unroll
   for (int u = 0; u < 8; ++u)
 #pragma unroll
-    for (int w = 0; w < 8; ++w) acc[u][w] = 0.f;
+    for (int w2 = 0; w2 < 4; ++w2) acc[u][w2] = f2_make(0.f, 0.f);
   const int nk = (d + kSK - 1) / kSK;
   load(0);
   store(0);
@@ -226,11 +227,13 @@ __global__ void __launch_bounds__(kSThreads) scores_kernel(const float* __restri
       const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][c][4 * tx]);
       const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][c][64 + 4 * tx]);
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      const f2 b[4] = {f2_make(b0.x, b0.y), f2_make(b0.z, b0.w), f2_make(b1.x, b1.y), f2_make(b1.z, b1.w)};
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
+      for (int u = 0; u < 8; ++u) {
+        const f2 au = f2_make(a[u], a[u]);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) acc[u][w] = fmaf(a[u], b[w], acc[u][w]);
+        for (int w2 = 0; w2 < 4; ++w2) acc[u][w2] = f2_fma(au, b[w2], acc[u][w2]);
+      }
     }
     if (kt + 1 < nk) store(buf ^ 1);
     __syncthreads();
@@ -240,10 +243,13 @@ __global__ void __launch_bounds__(kSThreads) scores_kernel(const float* __restri
     const int i = i0 + (u & 3) + 4 * ty + 64 * (u >> 2);
     if (i >= nb) continue;
     float* row = S + ((size_t)h * nb + i) * nb;
+    float v[8];
+#pragma unroll
+    for (int w2 = 0; w2 < 4; ++w2) f2_split(acc[u][w2], v[2 * w2], v[2 * w2 + 1]);
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
       const int j = j0 + (w & 3) + 4 * tx + 64 * (w >> 2);
-      if (j < nb) row[j] = acc[u][w] * scale;
+      if (j < nb) row[j] = v[w] * scale;
     }
   }
 }
