@@ -117,6 +117,30 @@ def test_pool_score_match_oracle(dtype, d, B, grid, heads):
     np.testing.assert_allclose(S.cpu().numpy(), oS, atol=2e-5, rtol=1e-4)
 
 
+def test_corrupt_permutation_entries_are_flagged_and_read_as_padding():
+    # the gather checks every permutation entry before it loads a row: entries outside
+    # [-1, N) are flagged (PRISM_DEV_BAD_INDEX) and read as padding (zero rows)
+    wl = small_workload((1, 1, 700), 2, 128, "bf16", 128)
+    Q, K, V = qkv(wl)
+    N, nb = wl.N, wl.nb
+    perm = np.arange(N, dtype=np.int32)
+    perm[5], perm[300] = N + 1000, -7
+    q, k, v = (to_dev(x, torch.bfloat16) for x in (Q, K, V))
+    qb, kb, vb = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    qbar = torch.empty(2, nb, 128, device=dev)
+    kbar = torch.empty_like(qbar)
+    S = torch.empty(2, nb, nb, device=dev)
+    P.prism_pool_score(q, k, v, torch.from_numpy(perm).to(dev), 128, qb, kb, vb, qbar, kbar, S)
+    assert P.status_check() == 2   # PRISM_DEV_BAD_INDEX
+    bad = np.zeros(N, bool)
+    bad[[5, 300]] = True
+    assert torch.count_nonzero(qb[torch.from_numpy(bad).to(dev)]) == 0
+    good = torch.from_numpy(~bad).to(dev)
+    assert torch.equal(qb[good], q[good]) and torch.equal(vb[good], v[good])
+    # a block without corrupt rows keeps its plain mean
+    np.testing.assert_allclose(qbar[:, 3].cpu().numpy(), Q[384:512].astype(np.float64).mean(0), atol=2e-6, rtol=1e-5)
+
+
 # --------------------------------------------------------------------- select
 @pytest.mark.parametrize("nb,rows,sp", [(10, 40, 0.75), (591, 300, 0.8), (1339, 120, 0.85), (2363, 60, 0.93),
                                         (64, 64, 0.0), (200, 50, 0.5)])
