@@ -257,7 +257,9 @@ int prism_score_select(const float* qbar, const float* kbar, int32_t Hh, int32_t
  *         are unspecified).
  * o_blk   out [N][Hh][d], row stride ld, same dtype as the inputs.
  * lse     out [Hh][N] fp32 (natural log).
- * ws      workspace (NULL = size query).
+ * ws      workspace (NULL = size query): on the tensor-core path, the order in which the
+ *         query blocks' CTAs are launched (Hh * nb int32): within each head, longest
+ *         kept list first; the order changes the schedule, never the results.
  * Limits: d in {64, 128}; B in {64, 128}; the tensor-core path needs d = B = 128.
  */
 int prism_bsa_fwd(const void* q_blk, const void* k_blk, const void* v_blk, int32_t dtype,
@@ -300,7 +302,10 @@ int prism_a2v_norm(const void* qv, const void* ka, const void* va, int32_t dtype
  * lse     [Hh][N] fp32 from prism_bsa_fwd.
  * blen    as prism_bsa_fwd (padding rows get zero gradients; their dO rows are ignored).
  * dq, dk, dv  out [N][Hh][d], row stride ld, same dtype.
- * ws      workspace (NULL = size query): transposed lists and row statistics.
+ * ws      workspace (NULL = size query): transposed lists, row statistics and, on the
+ *         tensor-core path, the launch orders of the query-block and key-block CTAs
+ *         (longest list first within each head).  With PRISM_BWD_FUSED=1 in the
+ *         environment the tensor-core path also holds an fp32 dQ accumulator.
  * Limits as prism_bsa_fwd.
  */
 int prism_bsa_bwd(const void* q_blk, const void* k_blk, const void* v_blk,
